@@ -1,0 +1,242 @@
+"""Seeded synthetic workloads for packed variable-length attention.
+
+This module only draws numbers: sequence lengths and bf16 N(0, 1) tensors of
+the shapes the pages' workloads have. It holds none of the method's
+arithmetic (no prefix sums, no packing, no attention), so both the CPU oracle
+and the CUDA path can take their inputs from here without sharing any of the
+computation they are compared on.
+
+Recipe (every draw on the CPU from ``torch.Generator().manual_seed(seed)``):
+lengths first, with ``torch.randint`` (inclusive bounds written as
+``randint(lo, hi + 1)``), then q, k, v in that order, each
+``torch.randn(..., dtype=float32)`` rounded to bf16.
+
+Image token counts are the Qwen-Image latent grid sizes: one token per 16x16
+pixel patch, so 768x768 -> 48*48 = 2304, 1024x1024 -> 4096, 1328x1328 -> 6889
+and 2048x2048 -> 16384 ("[Perf][qwen-image-edit] Skip attention-mask to avoid
+varlen path", Test Result: 16,384 tokens at 2048x2048, 16,384*2 for the edit
+model's noise + source latents, 6889 -> 6896 at 1328x1328).
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass, field
+from typing import List, Optional, Tuple
+
+import torch
+
+# Qwen-Image latent token counts for 768^2, 1024^2, 1328^2 and 2048^2 images.
+IMAGE_TOKENS = (2304, 4096, 6889, 16384)
+
+
+def image_tokens(height: int, width: int, patch: int = 16) -> int:
+    """Tokens of a (height x width) image: one per patch x patch pixel tile."""
+    return (height // patch) * (width // patch)
+
+
+@dataclass
+class VarlenWorkload:
+    """A packed batch: per-sequence query/key lengths and flat bf16 tensors.
+
+    q is [sum(lengths_q), H, D]; k and v are [sum(lengths_k), H, D], with the
+    tokens of sequence b stored contiguously in order b = 0, 1, ...  ``pad_rows``
+    extra rows (if any) sit after the last sequence and belong to no sequence.
+    """
+    name: str
+    lengths_q: List[int]
+    lengths_k: List[int]
+    H: int
+    D: int
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    seed: int
+    pad_rows: int = 0
+    meta: dict = field(default_factory=dict)
+
+    @property
+    def batch(self) -> int:
+        return len(self.lengths_q)
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / float(self.D) ** 0.5
+
+
+@dataclass
+class BlockWindowWorkload:
+    """Token2Wav-style block-window attention input, layout [batch, n, H, D]."""
+    name: str
+    batch: int
+    n: int
+    H: int
+    D: int
+    block: int
+    layers: List[Tuple[int, int]]  # (look_back, look_ahead) per DiT layer
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    seed: int
+
+    @property
+    def scale(self) -> float:
+        return 1.0 / float(self.D) ** 0.5
+
+
+@dataclass
+class PaddedWorkload:
+    """A padded batch [B, S_max, H, D]: sequence b's real tokens are rows
+    [0, lengths[b]) of slot b; the remaining rows are padding."""
+    name: str
+    lengths: List[int]
+    s_max: int
+    H: int
+    D: int
+    q: torch.Tensor
+    k: torch.Tensor
+    v: torch.Tensor
+    seed: int
+
+
+def _randn_bf16(g: torch.Generator, shape) -> torch.Tensor:
+    return torch.randn(*shape, generator=g, dtype=torch.float32).to(torch.bfloat16)
+
+
+def _qkv(g, tq, tk, H, D):
+    q = _randn_bf16(g, (tq, H, D))
+    k = _randn_bf16(g, (tk, H, D))
+    v = _randn_bf16(g, (tk, H, D))
+    return q, k, v
+
+
+# --------------------------------------------------------------------------
+# Lengths of the five workloads (drawn first from each workload's generator)
+# --------------------------------------------------------------------------
+
+def lengths_tiny() -> List[int]:
+    """Two packed sequences of 37 and 64 tokens, H=2, D=64, seed 0."""
+    return [37, 64]
+
+
+def lengths_mixed_res(g: torch.Generator) -> List[int]:
+    """Four joint text+image requests: text ~ U[16, 256] + 2304/4096/6889/16384."""
+    text = torch.randint(16, 257, (4,), generator=g).tolist()
+    return [t + img for t, img in zip(text, IMAGE_TOKENS)]
+
+
+def lengths_single_edit() -> List[int]:
+    """One edit request: 256 text + 2 * 16384 image tokens (noise + source)."""
+    return [256 + 2 * 16384]
+
+
+def lengths_cfg_batch(g: torch.Generator) -> Tuple[List[int], List[int]]:
+    """Eight requests, image tokens chosen uniformly from IMAGE_TOKENS; each
+    becomes two sequences (positive text + image, negative text + image) with
+    independent text lengths ~ U[8, 256].  Returns (lengths, request index)."""
+    img_idx = torch.randint(0, len(IMAGE_TOKENS), (8,), generator=g).tolist()
+    text = torch.randint(8, 257, (16,), generator=g).tolist()
+    lengths, owner = [], []
+    for r in range(8):
+        for s in range(2):
+            lengths.append(text[2 * r + s] + IMAGE_TOKENS[img_idx[r]])
+            owner.append(r)
+    return lengths, owner
+
+
+# --------------------------------------------------------------------------
+# Full workloads
+# --------------------------------------------------------------------------
+
+def tiny(seed: int = 0) -> VarlenWorkload:
+    g = torch.Generator().manual_seed(seed)
+    L = lengths_tiny()
+    q, k, v = _qkv(g, sum(L), sum(L), 2, 64)
+    return VarlenWorkload("tiny", L, list(L), 2, 64, q, k, v, seed)
+
+
+def mixed_res(seed: int = 2) -> VarlenWorkload:
+    g = torch.Generator().manual_seed(seed)
+    L = lengths_mixed_res(g)
+    q, k, v = _qkv(g, sum(L), sum(L), 24, 128)
+    return VarlenWorkload("mixed_res_mmdit", L, list(L), 24, 128, q, k, v, seed)
+
+
+def single_edit(seed: int = 3, pad_rows: int = 0) -> VarlenWorkload:
+    """The edit request; ``pad_rows`` > 0 adds that many trailing rows that
+    belong to no sequence (an auto-padded tail that trimming leaves out)."""
+    g = torch.Generator().manual_seed(seed)
+    L = lengths_single_edit()
+    T = sum(L) + pad_rows
+    q, k, v = _qkv(g, T, T, 24, 128)
+    return VarlenWorkload("single_edit" + ("_padded_tail" if pad_rows else ""),
+                          L, list(L), 24, 128, q, k, v, seed, pad_rows=pad_rows)
+
+
+def cfg_batch(seed: int = 5) -> VarlenWorkload:
+    g = torch.Generator().manual_seed(seed)
+    L, owner = lengths_cfg_batch(g)
+    q, k, v = _qkv(g, sum(L), sum(L), 24, 128)
+    return VarlenWorkload("cfg_dynamic_batch", L, list(L), 24, 128, q, k, v, seed,
+                          meta={"request_of_sequence": owner})
+
+
+TOKEN2WAV_LAYERS = [(0, 0)] * 19 + [(1, 1)] * 3
+
+
+def token2wav(n: int = 2400, seed: int = 4) -> BlockWindowWorkload:
+    """Token2Wav DiT block-window attention: batch 1, H=16, D=64, block 24;
+    19 own-block layers and 3 layers with one neighbour block each side."""
+    g = torch.Generator().manual_seed(seed)
+    shape = (1, n, 16, 64)
+    q = _randn_bf16(g, shape)
+    k = _randn_bf16(g, shape)
+    v = _randn_bf16(g, shape)
+    return BlockWindowWorkload("token2wav_block_window", 1, n, 16, 64, 24,
+                               list(TOKEN2WAV_LAYERS), q, k, v, seed)
+
+
+def padded(lengths: List[int], H: int, D: int, seed: int,
+           s_max: Optional[int] = None, name: str = "padded") -> PaddedWorkload:
+    """Padded [B, S_max, H, D] q/k/v for the given lengths (every row drawn,
+    padding rows included)."""
+    g = torch.Generator().manual_seed(seed)
+    s = max(lengths) if s_max is None else s_max
+    B = len(lengths)
+    q = _randn_bf16(g, (B, s, H, D))
+    k = _randn_bf16(g, (B, s, H, D))
+    v = _randn_bf16(g, (B, s, H, D))
+    return PaddedWorkload(name, list(lengths), s, H, D, q, k, v, seed)
+
+
+def mixed_res_padded(seed: int = 2) -> PaddedWorkload:
+    """The mixed-resolution batch in the padded layout the pack step reads."""
+    g = torch.Generator().manual_seed(seed)
+    L = lengths_mixed_res(g)
+    return padded(L, 24, 128, seed + 1000, name="mixed_res_mmdit_padded")
+
+
+def random_varlen(lengths_q: List[int], lengths_k: Optional[List[int]], H: int, D: int,
+                  seed: int, name: str = "random") -> VarlenWorkload:
+    """Arbitrary lengths (tests): flat q [sum Lq, H, D], k/v [sum Lk, H, D]."""
+    lk = list(lengths_q) if lengths_k is None else list(lengths_k)
+    g = torch.Generator().manual_seed(seed)
+    q, k, v = _qkv(g, sum(lengths_q), sum(lk), H, D)
+    return VarlenWorkload(name, list(lengths_q), lk, H, D, q, k, v, seed)
+
+
+def random_block_window(batch: int, n: int, H: int, D: int, block: int, seed: int,
+                        layers=None) -> BlockWindowWorkload:
+    g = torch.Generator().manual_seed(seed)
+    shape = (batch, n, H, D)
+    q = _randn_bf16(g, shape)
+    k = _randn_bf16(g, shape)
+    v = _randn_bf16(g, shape)
+    return BlockWindowWorkload(f"block_window_n{n}", batch, n, H, D, block,
+                               list(layers or [(0, 0)]), q, k, v, seed)
+
+
+VARLEN_CONFIGS = {
+    "tiny": tiny,
+    "mixed_res_mmdit": mixed_res,
+    "single_edit": single_edit,
+    "cfg_dynamic_batch": cfg_batch,
+}
