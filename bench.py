@@ -1,0 +1,443 @@
+"""Benchmark of the packed varlen attention hot path on GB300.
+
+One step = one pass of the whole path over one batch of the mixed-resolution
+joint text+image workload (4 requests: text U[16,256] + 2304/4096/6889/16384
+image tokens, H=24, D=128, bf16 N(0,1)):
+  cu_seqlens from lengths -> pack q, k, v (padded -> flat) -> varlen
+  attention -> unpack the output (flat -> padded).
+The Token2Wav block-window variant (22 layers, n=2400, H=16, D=64, block 24)
+is timed in the same run and reported under "block_window".
+
+Rank 0 prints one JSON line.  Under torchrun each rank runs its own batch
+(seed + rank) on its own GPU; no data moves between ranks (weak scaling);
+the timed region is bracketed by a barrier and the slowest rank's time is
+reported.
+
+--impl reference times the CPU oracle (fp64 NumPy) on a bounded sample of the
+same workload on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+import workloads  # noqa: E402
+
+METRIC = "packed varlen attention useful TFLOP/s and % of GB300 bf16 tensor peak"
+UNIT = "TFLOP/s"
+WORKLOAD = "mixed_res_mmdit"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+L2_FLUSH_BYTES = 512 << 20
+
+
+def _dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            raw = json.load(f)
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+    out = dict(FALLBACK_PEAKS)
+
+    def find(keys):
+        for k in keys:
+            if k in raw and isinstance(raw[k], (int, float)):
+                return float(raw[k])
+        return None
+    hbm = find(["hbm_gbs", "hbm_GBps", "hbm_gb_s"])
+    bf = find(["bf16_tflops", "bf16_TFLOPs"])
+    bfs = find(["bf16_tflops_sustained"])
+    if hbm:
+        out["hbm_gbs"] = hbm
+    if bf:
+        out["bf16_tflops"] = bf
+    if bfs:
+        out["bf16_tflops_sustained"] = bfs
+    return out, ("measured" if (hbm or bf) else "fallback")
+
+
+def _kernel_digest() -> str:
+    """Hash of the sources of the dominant kernel (ties an ncu traffic figure
+    to the code it was taken on)."""
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "packed_varlen_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        if name.startswith("attn_") or name.endswith(".cuh"):
+            with open(os.path.join(csrc, name), "rb") as f:
+                h.update(name.encode())
+                h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def _profiled_traffic(digest: str):
+    """DRAM bytes per launch of the attention kernel from the committed ncu
+    summary, if it was taken on the current kernel sources."""
+    path = os.path.join(ROOT, "profiles", "varlen_attn_mixed_res_mmdit.md")
+    try:
+        text = open(path).read()
+    except OSError:
+        return None
+    m_d = re.search(r"kernel_digest:\s*([0-9a-f]+)", text)
+    m_t = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
+    if m_d and m_t and m_d.group(1) == digest:
+        return float(m_t.group(1))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock/throttle samples taken while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _cpu_cores():
+    try:
+        return len(os.sched_getaffinity(0))
+    except AttributeError:
+        return os.cpu_count() or 1
+
+
+def block_window_flops(n, H, D, block, look_back, look_ahead):
+    """Useful FLOPs of one block-window layer: 4*H*D per allowed (query, key)
+    pair; a query of block i sees keys [(i-lb)*block, (i+la+1)*block) in [0, n)."""
+    pairs = 0
+    for i in range(-(-n // block)):
+        rows = min(n, (i + 1) * block) - i * block
+        keys = min(n, (i + look_ahead + 1) * block) - max(0, (i - look_back) * block)
+        pairs += rows * keys
+    return 4 * H * D * pairs
+
+
+def oracle_sample(w, rows_per_seq: int, seed: int = 0):
+    """Bounded oracle sample: ``rows_per_seq`` query rows of every sequence,
+    all heads.  Returns (seconds, useful FLOPs of the sample, description)."""
+    import oracle
+    rng = np.random.default_rng(seed)
+    cu = oracle.cu_seqlens_from_lengths(w.lengths_q)
+    rows, flops = [], 0
+    for b, L in enumerate(w.lengths_q):
+        r = np.sort(rng.choice(L, size=min(rows_per_seq, L), replace=False)) + cu[b]
+        rows.append(r)
+        flops += 4 * w.H * w.D * len(r) * w.lengths_k[b]
+    rows = np.concatenate(rows)
+    q, k, v = oracle.to_f64(w.q), oracle.to_f64(w.k), oracle.to_f64(w.v)
+    t0 = time.perf_counter()
+    oracle.varlen_attention(q, k, v, cu, cu, w.scale, rows=rows)
+    dt = time.perf_counter() - t0
+    desc = (f"{rows_per_seq} query rows per sequence x all {w.H} heads "
+            f"({len(rows)} rows) of the {w.name} batch, fp64 NumPy")
+    return dt, flops, desc
+
+
+def run_reference(args):
+    ws, rank, _ = _dist_env()
+    if rank != 0:
+        return 0
+    w = workloads.mixed_res(seed=2)
+    rows = args.ref_rows
+    for _ in range(args.warmup):
+        oracle_sample(w, rows)
+    times, flops, desc = [], 0, ""
+    for i in range(args.steps):
+        dt, flops, desc = oracle_sample(w, rows, seed=i)
+        times.append(dt)
+    total = sum(times)
+    value = flops * args.steps / total / 1e12
+    cores = _cpu_cores()
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+        "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": WORKLOAD, "batch": len(w.lengths_q), "H": w.H, "D": w.D,
+                   "tokens": sum(w.lengths_q), "sample": desc},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
+                         "sample": desc},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import packed_varlen_gb300 as pv
+
+    ws, rank, local = _dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    pv.load_library()
+    pv.get_device_status()
+
+    # ---- inputs: this rank's padded batch, resident in HBM -------------------
+    pw = workloads.mixed_res_padded(seed=2 + 1000 * rank)
+    L = pw.lengths
+    T, H, D, B, S = sum(L), pw.H, pw.D, len(L), pw.s_max
+    flops = 4 * H * D * sum(x * x for x in L)
+    stream = torch.cuda.current_stream()
+    q_pad, k_pad, v_pad = pw.q.to(dev), pw.k.to(dev), pw.v.to(dev)
+    lengths = torch.tensor(L, dtype=torch.int32, device=dev)
+    cu = torch.empty(B + 1, dtype=torch.int32, device=dev)
+    qf = torch.empty(T, H, D, dtype=torch.bfloat16, device=dev)
+    kf, vf, of = torch.empty_like(qf), torch.empty_like(qf), torch.empty_like(qf)
+    out_pad = torch.zeros_like(q_pad)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    scale = 1.0 / math.sqrt(D)
+
+    attn_ev = []
+
+    def step(record=False):
+        pv.cu_seqlens_from_lengths(lengths, out=cu)
+        pv.pack(q_pad, cu, T, out=qf)
+        pv.pack(k_pad, cu, T, out=kf)
+        pv.pack(v_pad, cu, T, out=vf)
+        if record:
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+        pv.varlen_attn_fwd(qf, kf, vf, cu, cu, max(L), max(L), scale=scale, out=of)
+        if record:
+            e1.record(stream)
+            attn_ev.append((e0, e1))
+        pv.unpack(of, cu, out_pad)
+
+    launches_per_step = 6
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    if pv.get_device_status() != 0:
+        raise RuntimeError("device status error during warm-up")
+
+    # ---- timed: K steps, L2 flushed between steps (outside the events) ------
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    if dist:
+        dist.barrier()
+    torch.cuda.synchronize()
+    step_ev = []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        step(record=True)
+        e1.record(stream)
+        step_ev.append((e0, e1))
+    torch.cuda.synchronize()
+    if dist:
+        dist.barrier()
+    clocks = sampler.stop()
+    step_ms = [a.elapsed_time(b) for a, b in step_ev]
+    attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
+    total_ms = sum(step_ms)
+    if dist:
+        t = torch.tensor([total_ms], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    value = flops * ws * args.steps / (total_ms * 1e-3) / 1e12
+
+    # ---- end to end: host buffers in, host result out ----------------------
+    hq, hk, hv = (t.pin_memory() for t in (pw.q, pw.k, pw.v))
+    hlen = torch.tensor(L, dtype=torch.int32).pin_memory()
+    hout = torch.empty_like(pw.q).pin_memory()
+    h2d = 3 * hq.numel() * hq.element_size() + hlen.numel() * 4
+    d2h = hout.numel() * hout.element_size()
+
+    def e2e_step():
+        lengths.copy_(hlen, non_blocking=True)
+        q_pad.copy_(hq, non_blocking=True)
+        k_pad.copy_(hk, non_blocking=True)
+        v_pad.copy_(hv, non_blocking=True)
+        step()
+        hout.copy_(out_pad, non_blocking=True)
+
+    for _ in range(2):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for _ in range(max(3, min(args.steps, 10))):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        e2e_step()
+        e1.record(stream)
+        torch.cuda.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
+    e2e_total = sum(e2e_ms)
+    if dist:
+        t = torch.tensor([e2e_total / len(e2e_ms)], device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_mean = float(t.item())
+    else:
+        e2e_mean = e2e_total / len(e2e_ms)
+    e2e_value = flops * ws / (e2e_mean * 1e-3) / 1e12
+
+    # ---- block-window variant (Token2Wav), timed per layer -------------------
+    bw = workloads.token2wav()
+    bq, bk, bv = bw.q.to(dev), bw.k.to(dev), bw.v.to(dev)
+    bo = torch.empty_like(bq)
+    for _ in range(3):
+        for lb, la in bw.layers:
+            pv.block_window_attn_fwd(bq, bk, bv, bw.block, lb, la, out=bo)
+    torch.cuda.synchronize()
+    per_layer = {}
+    for lb, la in sorted(set(bw.layers)):
+        ts = []
+        for _ in range(20):
+            flush.zero_()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            pv.block_window_attn_fwd(bq, bk, bv, bw.block, lb, la, out=bo)
+            e1.record(stream)
+            ts.append((e0, e1))
+        torch.cuda.synchronize()
+        per_layer[(lb, la)] = statistics.median(a.elapsed_time(b) for a, b in ts)
+    bw_bytes = 4 * bq.numel() * 2   # q, k, v read once, out written once
+    total_bw_us = sum(per_layer[l] for l in bw.layers) * 1e3
+    bw_flops = sum(block_window_flops(bw.n, bw.H, bw.D, bw.block, lb, la) for lb, la in bw.layers)
+
+    if pv.get_device_status() != 0:
+        raise RuntimeError("device status error during the timed run")
+
+    peaks, peak_src = _peaks()
+    attn_mean_ms = statistics.mean(attn_ms)
+    achieved = flops / (attn_mean_ms * 1e-3) / 1e12
+    digest = _kernel_digest()
+    traffic = _profiled_traffic(digest)
+    result = None
+    if rank == 0:
+        cpu = None
+        if ws == 1 and not args.no_cpu_baseline:
+            w = workloads.mixed_res(seed=2)
+            dt, sflops, desc = oracle_sample(w, args.cpu_rows)
+            cpu = {"value": sflops / dt / 1e12, "unit": UNIT, "cores": _cpu_cores(),
+                   "kind": "oracle", "sample": desc, "seconds": dt}
+        result = {
+            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+            "steps": args.steps, "warmup": max(3, args.warmup),
+            "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "batch": B, "lengths": L, "tokens": T, "H": H,
+                       "D": D, "s_max": S, "useful_flops_per_step": flops,
+                       "step": "cu_seqlens + pack q,k,v + varlen attention + unpack",
+                       "l2": "flushed between timed steps (512 MB write outside the events); "
+                             "padded inputs 3 x %.0f MB also exceed L2"
+                             % (q_pad.numel() * 2 / 2**20),
+                       "parallelism": f"{ws} independent batches (one per GPU)"},
+            "pct_of_peak": 100.0 * value / peaks["bf16_tflops"],
+            "roofline": {"kernel": "varlen_attn_fwd", "bound": "tensor",
+                         "achieved": achieved, "peak": peaks["bf16_tflops"],
+                         "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                         "peak_source": f"{peak_src} bf16 dense (burst)",
+                         "launch_ms": attn_mean_ms, "traffic": traffic,
+                         "kernel_digest": digest},
+            "cpu_baseline": cpu,
+            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_mean},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+            "block_window": {
+                "workload": "token2wav n=2400 H=16 D=64 block=24, 19 x (0,0) + 3 x (1,1) layers",
+                "us_per_layer": {f"{lb},{la}": 1e3 * ms for (lb, la), ms in per_layer.items()},
+                "us_all_layers": total_bw_us,
+                "gbs_own_block_layer": bw_bytes / (per_layer[(0, 0)] * 1e-3) / 1e9,
+                "hbm_frac_own_block_layer": bw_bytes / (per_layer[(0, 0)] * 1e-3) / 1e9
+                / peaks["hbm_gbs"],
+                "useful_tflops": bw_flops / (total_bw_us * 1e-6) / 1e12,
+                "launches": len(bw.layers)},
+        }
+        print(json.dumps(result), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--cpu-rows", type=int, default=2048,
+                    help="query rows per sequence in the CPU-oracle baseline sample")
+    ap.add_argument("--ref-rows", type=int, default=128,
+                    help="query rows per sequence per step of --impl reference")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

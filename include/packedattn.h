@@ -1,0 +1,197 @@
+/*
+ * packedattn.h -- C ABI of libpackedattn, forward attention over flat-packed
+ * variable-length sequences on NVIDIA GB300 (sm_103a).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Every tensor argument is a DEVICE pointer to caller-owned memory.  The
+ *   library never allocates, frees or keeps a reference to caller memory;
+ *   outputs are written asynchronously on `stream` and are valid once the
+ *   stream has reached that point.
+ * - Attention tensors are bf16, token-major and contiguous: element
+ *   (token t, head h, dim d) sits at offset (t * H + h) * D + d.
+ * - Sequence boundaries are int32 "cu_seqlens" arrays of batch + 1 entries:
+ *   cu[0] = 0, non-decreasing, sequence b owns rows [cu[b], cu[b+1]).
+ * - Every call returns a pa_status.  Arguments are checked on the host before
+ *   anything is launched; a failed check launches nothing.  Nothing blocks
+ *   the host, synchronizes the device or copies device -> host, except
+ *   pa_get_device_status.  Nothing aborts, traps or throws.
+ * - Checks that need the contents of device arrays (cu_seqlens monotone and
+ *   consistent with the totals, lengths within max_q / max_k) run inside the
+ *   kernels: a violation records an error code in a per-device status word
+ *   (read with pa_get_device_status) and the offending work is skipped.
+ * - Every kernel wait on the GPU is bounded; a wait that runs out records
+ *   PA_DEVICE_ERR_TIMEOUT in the status word and the kernel returns.
+ * - `stream` is a cudaStream_t (NULL = the legacy default stream).
+ */
+#ifndef PACKEDATTN_H
+#define PACKEDATTN_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct CUstream_st *pa_stream_t; /* identical to cudaStream_t */
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,  /* null pointer, negative or zero size, non-finite scale */
+  PA_ERR_UNSUPPORTED = 2,  /* valid but not implemented: D not 64/128, too many sequences */
+  PA_ERR_MISALIGNED = 3,   /* a pointer or row pitch breaks the 16-byte rule */
+  PA_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed (launch, tensor map) */
+  PA_ERR_DEVICE = 5        /* pa_get_device_status found a recorded device error */
+} pa_status;
+
+/* Device-side error codes recorded in the status word (first error wins). */
+#define PA_DEVICE_OK 0
+#define PA_DEVICE_ERR_CU_SEQLENS 1   /* cu[0] != 0, decreasing, or cu[batch] != total */
+#define PA_DEVICE_ERR_MAX_LEN 2      /* a sequence longer than max_q / max_k / s_max */
+#define PA_DEVICE_ERR_TIMEOUT 3      /* a bounded pipeline wait ran out */
+#define PA_DEVICE_ERR_LENGTH 4       /* a negative length, or a sum above INT32_MAX, in
+                                        pa_cu_seqlens_from_lengths */
+#define PA_DEVICE_ERR_CAPACITY 5     /* pa_varlen_work_order: more items than capacity */
+
+/* Largest batch (number of packed sequences) the attention kernels accept. */
+#define PA_MAX_BATCH 1024
+
+/* Query rows per work item of pa_varlen_attn_fwd. */
+#define PA_VARLEN_TILE_M 128
+
+/*
+ * pa_varlen_attn_fwd -- non-causal softmax attention over a flat packed batch.
+ *
+ * Defined by the flat varlen attention path of "[Perf][Diffusion][Qwen-Image]
+ * Replace per-bucket varlen loop with flat varlen attention for mixfusion"
+ * (Key changes: AttentionMetadata with q_cu_seqlens / kv_cu_seqlens /
+ * max_q_len / max_kv_len, packed [total_tokens, heads, head_dim] Q/K/V, no
+ * attention mask, no padded tokens) and "feat: Support dynamic batching for
+ * heterogeneous diffusion requests" (AttentionMetadata: tokens of one request
+ * never attend to another's).  For sequence b, head h and query row i of b:
+ *   out[i,h,:] = sum_j softmax_j(scale * <q[i,h,:], k[j,h,:]>) * v[j,h,:]
+ * over the key rows j of the same sequence only.  A sequence with queries but
+ * no keys gets all-zero output rows.
+ *
+ * q     [total_q, H, D] bf16      k, v [total_k, H, D] bf16
+ * out   [total_q, H, D] bf16, written only at rows that belong to a sequence
+ *       (rows >= cu_seqlens_q[batch] are left untouched)
+ * cu_seqlens_q / cu_seqlens_k: device int32 [batch + 1]
+ * batch in [1, PA_MAX_BATCH]; total_q/total_k >= cu[batch] (extra rows are
+ * padding that is neither read as keys nor written); max_q / max_k bound every
+ * sequence length; H >= 1; D in {64, 128}; scale finite (1/sqrt(D) is usual).
+ * q, k, v, out must be 16-byte aligned.
+ * Deterministic: every output row is computed by one CTA in a fixed order, so
+ * a sequence's result does not depend on which other sequences share the
+ * batch (bit-identical to running it alone).
+ */
+pa_status pa_varlen_attn_fwd(const void *q, const void *k, const void *v, void *out,
+                             const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                             int32_t batch, int32_t total_q, int32_t total_k,
+                             int32_t max_q, int32_t max_k, int32_t H, int32_t D,
+                             float scale, pa_stream_t stream);
+
+/*
+ * pa_block_window_attn_fwd -- block-local attention of the Token2Wav DiT.
+ *
+ * Defined by "[Perf][Model] Use block-sparse attention in Qwen2.5-Omni
+ * Token2Wav DiT" (Purpose; Change: the same result as dense attention under
+ * the block-difference mask).  Frames are grouped in blocks of `block`; query
+ * i attends to key j iff j < n and
+ *   -look_back <= floor(j / block) - floor(i / block) <= look_ahead
+ * (look_back blocks before, look_ahead blocks after).  Whether any masking is
+ * needed is decided from these integers on the host; nothing is read back
+ * from the device.
+ *
+ * q, k, v, out [batch, n, H, D] bf16 contiguous (token-major per batch entry).
+ * batch >= 1, n >= 1, block >= 1, look_back >= 0, look_ahead >= 0, H >= 1,
+ * D in {64, 128}, scale finite; pointers 16-byte aligned.
+ */
+pa_status pa_block_window_attn_fwd(const void *q, const void *k, const void *v, void *out,
+                                   int32_t batch, int32_t n, int32_t block,
+                                   int32_t look_back, int32_t look_ahead,
+                                   int32_t H, int32_t D, float scale, pa_stream_t stream);
+
+/*
+ * pa_cu_seqlens_from_lengths -- cu[0] = 0, cu[b+1] = cu[b] + lengths[b].
+ *
+ * The flat path's boundaries come from each request's real token count
+ * ("[Perf][Diffusion][Qwen-Image] Replace per-bucket varlen loop with flat
+ * varlen attention for mixfusion", Key changes: cu_seqlens built from real
+ * text lengths via mask.sum).  lengths: device int32 [batch]; cu: device int32
+ * [batch + 1].  batch >= 1.  A negative length records
+ * PA_DEVICE_ERR_LENGTH and is treated as 0.
+ */
+pa_status pa_cu_seqlens_from_lengths(const int32_t *lengths, int32_t *cu, int32_t batch,
+                                     pa_stream_t stream);
+
+/*
+ * pa_pack -- copy the real rows of a padded batch into the flat layout.
+ *
+ * Only real tokens enter the packed tensor ("feat: Support dynamic batching
+ * for heterogeneous diffusion requests", How batching works).  padded is
+ * [batch, s_max, row_bytes] bytes, flat is [total, row_bytes]; row r of
+ * sequence b (r < cu[b+1] - cu[b]) goes from padded[b, r] to flat[cu[b] + r].
+ * Flat rows >= cu[batch] are not touched.  cu: device int32 [batch + 1].
+ * batch >= 1, s_max >= 0, total >= 0, row_bytes > 0 and a multiple of 16;
+ * pointers 16-byte aligned.  A sequence longer than s_max records
+ * PA_DEVICE_ERR_MAX_LEN, boundaries outside [0, total] or decreasing record
+ * PA_DEVICE_ERR_CU_SEQLENS; such a sequence is skipped.
+ */
+pa_status pa_pack(const void *padded, void *flat, const int32_t *cu, int32_t batch,
+                  int32_t s_max, int32_t total, int64_t row_bytes, pa_stream_t stream);
+
+/*
+ * pa_unpack -- the inverse scatter: flat[cu[b] + r] -> padded[b, r] for
+ * r < cu[b+1] - cu[b]; padding rows of `padded` are left untouched (output
+ * unpacked by cu_seqlens, same page as pa_cu_seqlens_from_lengths).
+ * Same argument rules as pa_pack.
+ */
+pa_status pa_unpack(const void *flat, void *padded, const int32_t *cu, int32_t batch,
+                    int32_t s_max, int32_t total, int64_t row_bytes, pa_stream_t stream);
+
+/*
+ * pa_varlen_num_work_items -- host-side count of attention work items,
+ * sum_b H * ceil(Lq[b] / tile_m), from HOST copies of cu_seqlens_q.
+ * Returns -1 on invalid arguments.
+ */
+int64_t pa_varlen_num_work_items(const int32_t *cu_seqlens_q_host, int32_t batch,
+                                 int32_t H, int32_t tile_m);
+
+/*
+ * pa_varlen_work_order -- the order in which the attention kernel visits its
+ * work items, written by the same device code the kernel schedules with.
+ *
+ * Sequences are taken longest key length first (equal lengths: lower index
+ * first); within a sequence heads in order, within a head query tiles of
+ * tile_m rows in order.  The largest request dominates a mixed batch and the
+ * old per-bucket loop left bubbles ("[Perf][Diffusion][Qwen-Image] Replace
+ * per-bucket varlen loop ...", Purpose), so the longest work starts first.
+ * items: device int32 [capacity, 3] receiving (sequence, head, q_tile) for
+ * item 0, 1, ...; when there are more items than capacity, the first
+ * `capacity` are written and PA_DEVICE_ERR_CAPACITY is recorded.  Boundaries
+ * are checked as in pa_varlen_attn_fwd (without totals or maxima); a bad
+ * sequence gets no items.  batch in [1, PA_MAX_BATCH], H >= 1, tile_m >= 1.
+ * PA_VARLEN_TILE_M is the tile the attention kernel uses.
+ */
+pa_status pa_varlen_work_order(const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                               int32_t batch, int32_t H, int32_t tile_m,
+                               int32_t *items, int64_t capacity, pa_stream_t stream);
+
+/*
+ * pa_get_device_status -- synchronize the current device, then read and
+ * clear its status word.  *code receives PA_DEVICE_OK or the first
+ * PA_DEVICE_ERR_* recorded since the last call.  Returns PA_ERR_DEVICE when
+ * an error was recorded, PA_ERR_CUDA when the synchronize fails.  For tests
+ * and debugging: it blocks the host.
+ */
+pa_status pa_get_device_status(int32_t *code);
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *pa_status_string(pa_status status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PACKEDATTN_H */

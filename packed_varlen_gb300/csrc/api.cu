@@ -1,0 +1,310 @@
+// C-ABI layer of libpackedattn: host-side argument checks, the per-device
+// status word, and the small kernels of the packed layout (boundaries, pack,
+// unpack, work order).  Attention kernels live in their own translation units.
+#include <cuda_runtime.h>
+#include <math.h>
+#include <stdint.h>
+
+#include "internal.h"
+#include "sched.cuh"
+
+namespace pa {
+namespace {
+
+// First device-side error since the last pa_get_device_status (0 = none).
+__device__ int32_t g_status_word;
+
+constexpr int kMaxDevices = 64;
+int32_t *g_status_addr[kMaxDevices];
+int g_num_sms[kMaxDevices];
+
+// Device address of the status word and SM count of the current device.
+cudaError_t device_context(int32_t **status, int *num_sms) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  if (g_status_addr[dev] == nullptr) {
+    void *addr = nullptr;
+    e = cudaGetSymbolAddress(&addr, g_status_word);
+    if (e != cudaSuccess) return e;
+    int sms = 0;
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    g_num_sms[dev] = sms;
+    g_status_addr[dev] = static_cast<int32_t *>(addr);
+  }
+  *status = g_status_addr[dev];
+  *num_sms = g_num_sms[dev];
+  return cudaSuccess;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
+
+// ---------------------------------------------------------------------------
+// cu_seqlens from lengths: one CTA, chunked block scan with an int64 carry.
+// ---------------------------------------------------------------------------
+constexpr int kScanThreads = 1024;
+
+__global__ void __launch_bounds__(kScanThreads)
+    cu_seqlens_kernel(const int32_t *__restrict__ lengths, int32_t *__restrict__ cu, int batch,
+                      int32_t *status) {
+  __shared__ int64_t warp_sums[kScanThreads / 32];
+  __shared__ int64_t carry_s;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  if (tid == 0) {
+    carry_s = 0;
+    cu[0] = 0;
+  }
+  __syncthreads();
+  bool overflow = false;
+  for (int base = 0; base < batch; base += kScanThreads) {
+    const int idx = base + tid;
+    int64_t x = 0;
+    if (idx < batch) {
+      const int32_t L = lengths[idx];
+      if (L < 0) record_error(status, PA_DEVICE_ERR_LENGTH);
+      x = L < 0 ? 0 : L;
+    }
+    int64_t incl = x;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int64_t y = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += y;
+    }
+    if (lane == 31) warp_sums[warp] = incl;
+    __syncthreads();
+    if (warp == 0) {
+      int64_t w = warp_sums[lane];
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, w, off);
+        if (lane >= off) w += y;
+      }
+      warp_sums[lane] = w;  // inclusive over warps
+    }
+    __syncthreads();
+    const int64_t before = carry_s + (warp > 0 ? warp_sums[warp - 1] : 0);
+    const int64_t val = before + incl;
+    if (idx < batch) {
+      if (val > INT32_MAX) overflow = true;
+      cu[idx + 1] = static_cast<int32_t>(val > INT32_MAX ? INT32_MAX : val);
+    }
+    __syncthreads();
+    if (tid == 0) carry_s += warp_sums[31];
+    __syncthreads();
+  }
+  if (overflow) record_error(status, PA_DEVICE_ERR_LENGTH);
+}
+
+// ---------------------------------------------------------------------------
+// pack / unpack: one padded row per loop step of a CTA, 16-byte vectors.
+// ---------------------------------------------------------------------------
+constexpr int kCopyThreads = 256;
+
+template <bool kPack>
+__global__ void __launch_bounds__(kCopyThreads)
+    repack_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
+                  const int32_t *__restrict__ cu, int batch, int s_max, int total,
+                  int64_t row_vecs, int32_t *status) {
+  const int b = blockIdx.y;
+  const int c0 = __ldg(cu + b), c1 = __ldg(cu + b + 1);
+  const bool ok = c0 >= 0 && c0 <= c1 && c1 <= total && (b > 0 || c0 == 0);
+  if (!ok || c1 - c0 > s_max) {
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+      record_error(status, ok ? PA_DEVICE_ERR_MAX_LEN : PA_DEVICE_ERR_CU_SEQLENS);
+    return;
+  }
+  const int L = c1 - c0;
+  for (int r = blockIdx.x; r < L; r += gridDim.x) {
+    const int64_t padded_row = static_cast<int64_t>(b) * s_max + r;
+    const int64_t flat_row = static_cast<int64_t>(c0) + r;
+    const uint4 *s = src + (kPack ? padded_row : flat_row) * row_vecs;
+    uint4 *d = dst + (kPack ? flat_row : padded_row) * row_vecs;
+    for (int64_t i = threadIdx.x; i < row_vecs; i += kCopyThreads) d[i] = __ldg(s + i);
+  }
+}
+
+// ---------------------------------------------------------------------------
+// Work order: the attention scheduler's list, written out.
+// ---------------------------------------------------------------------------
+constexpr int kOrderThreads = 256;
+
+__global__ void __launch_bounds__(kOrderThreads)
+    work_order_kernel(const int32_t *__restrict__ cu_q, const int32_t *__restrict__ cu_k,
+                      int batch, int H, int tile_m, int32_t *__restrict__ items,
+                      int64_t capacity, int32_t *status) {
+  extern __shared__ int32_t sm[];
+  int32_t *order = sm, *prefix = sm + batch, *tmp_lq = prefix + batch + 1,
+          *tmp_lk = tmp_lq + batch;
+  sched_build(order, prefix, tmp_lq, tmp_lk, cu_q, cu_k, batch, H, tile_m, INT32_MAX,
+              INT32_MAX, INT32_MAX, INT32_MAX, status, true);
+  const int n_items = prefix[batch];
+  if (n_items > capacity && threadIdx.x == 0) record_error(status, PA_DEVICE_ERR_CAPACITY);
+  const int64_t n_write = n_items < capacity ? n_items : capacity;
+  for (int64_t i = threadIdx.x; i < n_write; i += kOrderThreads) {
+    const WorkItem w = sched_item(order, prefix, batch, H, static_cast<int>(i));
+    items[3 * i + 0] = w.seq;
+    items[3 * i + 1] = w.head;
+    items[3 * i + 2] = w.tile;
+  }
+}
+
+pa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+const char *pa_status_string(pa_status s) {
+  switch (s) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_MISALIGNED: return "PA_ERR_MISALIGNED";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    case PA_ERR_DEVICE: return "PA_ERR_DEVICE";
+  }
+  return "PA_ERR_UNKNOWN";
+}
+
+pa_status pa_varlen_attn_fwd(const void *q, const void *k, const void *v, void *out,
+                             const int32_t *cu_seqlens_q, const int32_t *cu_seqlens_k,
+                             int32_t batch, int32_t total_q, int32_t total_k, int32_t max_q,
+                             int32_t max_k, int32_t H, int32_t D, float scale,
+                             pa_stream_t stream) {
+  if (!q || !k || !v || !out || !cu_seqlens_q || !cu_seqlens_k) return PA_ERR_INVALID_ARG;
+  if (batch < 1 || total_q < 0 || total_k < 0 || max_q < 0 || max_k < 0 || H < 1 || D < 1)
+    return PA_ERR_INVALID_ARG;
+  if (!isfinite(scale)) return PA_ERR_INVALID_ARG;
+  if (batch > PA_MAX_BATCH || (D != 64 && D != 128) || H > 65535) return PA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) ||
+      !aligned4(cu_seqlens_q) || !aligned4(cu_seqlens_k))
+    return PA_ERR_MISALIGNED;
+  if (total_q == 0 || max_q == 0) return PA_OK;  // no query rows: nothing to write
+  VarlenArgs a{q, k, v, out, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, max_q,
+               max_k, H, D, scale, nullptr, 0};
+  cudaError_t e = device_context(&a.status, &a.num_sms);
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  return from_cuda(launch_varlen_attn(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pa_status pa_block_window_attn_fwd(const void *q, const void *k, const void *v, void *out,
+                                   int32_t batch, int32_t n, int32_t block, int32_t look_back,
+                                   int32_t look_ahead, int32_t H, int32_t D, float scale,
+                                   pa_stream_t stream) {
+  if (!q || !k || !v || !out) return PA_ERR_INVALID_ARG;
+  if (batch < 1 || n < 1 || block < 1 || look_back < 0 || look_ahead < 0 || H < 1 || D < 1)
+    return PA_ERR_INVALID_ARG;
+  if (!isfinite(scale)) return PA_ERR_INVALID_ARG;
+  if ((D != 64 && D != 128) || H > 65535 || batch > 65535) return PA_ERR_UNSUPPORTED;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return PA_ERR_MISALIGNED;
+  BlockWindowArgs a{q, k, v, out, batch, n, block, look_back, look_ahead, H, D, scale,
+                    nullptr, 0};
+  cudaError_t e = device_context(&a.status, &a.num_sms);
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  return from_cuda(launch_block_window_attn(a, reinterpret_cast<cudaStream_t>(stream)));
+}
+
+pa_status pa_cu_seqlens_from_lengths(const int32_t *lengths, int32_t *cu, int32_t batch,
+                                     pa_stream_t stream) {
+  if (!lengths || !cu || batch < 1) return PA_ERR_INVALID_ARG;
+  if (!aligned4(lengths) || !aligned4(cu)) return PA_ERR_MISALIGNED;
+  int32_t *status;
+  int sms;
+  if (device_context(&status, &sms) != cudaSuccess) return PA_ERR_CUDA;
+  cu_seqlens_kernel<<<1, kScanThreads, 0, reinterpret_cast<cudaStream_t>(stream)>>>(
+      lengths, cu, batch, status);
+  return from_cuda(cudaGetLastError());
+}
+
+static pa_status repack(bool is_pack, const void *src, void *dst, const int32_t *cu,
+                        int32_t batch, int32_t s_max, int32_t total, int64_t row_bytes,
+                        pa_stream_t stream) {
+  if (!src || !dst || !cu || batch < 1 || s_max < 0 || total < 0 || row_bytes <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (batch > 65535) return PA_ERR_UNSUPPORTED;
+  if ((row_bytes & 15) != 0 || !aligned16(src) || !aligned16(dst) || !aligned4(cu))
+    return PA_ERR_MISALIGNED;
+  if (s_max == 0) return PA_OK;
+  int32_t *status;
+  int sms;
+  if (device_context(&status, &sms) != cudaSuccess) return PA_ERR_CUDA;
+  // enough CTAs to cover the GPU several times; each strides over its rows
+  int per_seq = (sms * 8 + batch - 1) / batch;
+  if (per_seq > s_max) per_seq = s_max;
+  if (per_seq < 1) per_seq = 1;
+  dim3 grid(per_seq, batch);
+  const int64_t vecs = row_bytes / 16;
+  auto st = reinterpret_cast<cudaStream_t>(stream);
+  if (is_pack)
+    repack_kernel<true><<<grid, kCopyThreads, 0, st>>>(static_cast<const uint4 *>(src),
+                                                        static_cast<uint4 *>(dst), cu, batch,
+                                                        s_max, total, vecs, status);
+  else
+    repack_kernel<false><<<grid, kCopyThreads, 0, st>>>(static_cast<const uint4 *>(src),
+                                                         static_cast<uint4 *>(dst), cu, batch,
+                                                         s_max, total, vecs, status);
+  return from_cuda(cudaGetLastError());
+}
+
+pa_status pa_pack(const void *padded, void *flat, const int32_t *cu, int32_t batch,
+                  int32_t s_max, int32_t total, int64_t row_bytes, pa_stream_t stream) {
+  return repack(true, padded, flat, cu, batch, s_max, total, row_bytes, stream);
+}
+
+pa_status pa_unpack(const void *flat, void *padded, const int32_t *cu, int32_t batch,
+                    int32_t s_max, int32_t total, int64_t row_bytes, pa_stream_t stream) {
+  return repack(false, flat, padded, cu, batch, s_max, total, row_bytes, stream);
+}
+
+int64_t pa_varlen_num_work_items(const int32_t *cu_q_host, int32_t batch, int32_t H,
+                                 int32_t tile_m) {
+  if (!cu_q_host || batch < 1 || H < 1 || tile_m < 1) return -1;
+  int64_t n = 0;
+  for (int b = 0; b < batch; ++b) {
+    const int64_t L = static_cast<int64_t>(cu_q_host[b + 1]) - cu_q_host[b];
+    if (L < 0) return -1;
+    n += static_cast<int64_t>(H) * ((L + tile_m - 1) / tile_m);
+  }
+  return n;
+}
+
+pa_status pa_varlen_work_order(const int32_t *cu_q, const int32_t *cu_k, int32_t batch,
+                               int32_t H, int32_t tile_m, int32_t *items, int64_t capacity,
+                               pa_stream_t stream) {
+  if (!cu_q || !cu_k || !items || batch < 1 || H < 1 || tile_m < 1 || capacity < 0)
+    return PA_ERR_INVALID_ARG;
+  if (batch > PA_MAX_BATCH) return PA_ERR_UNSUPPORTED;
+  if (!aligned4(cu_q) || !aligned4(cu_k) || !aligned4(items)) return PA_ERR_MISALIGNED;
+  int32_t *status;
+  int sms;
+  if (device_context(&status, &sms) != cudaSuccess) return PA_ERR_CUDA;
+  const size_t smem = sizeof(int32_t) * (4 * static_cast<size_t>(batch) + 1);
+  work_order_kernel<<<1, kOrderThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(
+      cu_q, cu_k, batch, H, tile_m, items, capacity, status);
+  return from_cuda(cudaGetLastError());
+}
+
+pa_status pa_get_device_status(int32_t *code) {
+  if (!code) return PA_ERR_INVALID_ARG;
+  int32_t *status;
+  int sms;
+  if (device_context(&status, &sms) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaDeviceSynchronize() != cudaSuccess) return PA_ERR_CUDA;
+  int32_t v = 0;
+  if (cudaMemcpy(&v, status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return PA_ERR_CUDA;
+  const int32_t zero = 0;
+  if (cudaMemcpy(status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+    return PA_ERR_CUDA;
+  *code = v;
+  return v == 0 ? PA_OK : PA_ERR_DEVICE;
+}
+
+}  // extern "C"

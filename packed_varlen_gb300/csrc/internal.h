@@ -1,0 +1,36 @@
+// Internal interface between the C-ABI layer (api.cu) and the kernel
+// translation units.  Not installed, not part of the ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/packedattn.h"
+
+namespace pa {
+
+// Everything an attention launch needs; filled and validated by api.cu.
+struct VarlenArgs {
+  const void *q, *k, *v;
+  void *out;
+  const int32_t *cu_q, *cu_k;
+  int32_t batch, total_q, total_k, max_q, max_k, H, D;
+  float scale;
+  int32_t *status;  // device address of the per-device status word
+  int num_sms;
+};
+
+struct BlockWindowArgs {
+  const void *q, *k, *v;
+  void *out;
+  int32_t batch, n, block, look_back, look_ahead, H, D;
+  float scale;
+  int32_t *status;
+  int num_sms;
+};
+
+// Launchers: return cudaSuccess or the launch error.
+cudaError_t launch_varlen_attn(const VarlenArgs &a, cudaStream_t stream);
+cudaError_t launch_block_window_attn(const BlockWindowArgs &a, cudaStream_t stream);
+
+}  // namespace pa

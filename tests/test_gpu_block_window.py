@@ -1,0 +1,76 @@
+"""Parity of the CUDA block-window attention with the dense block-difference
+mask oracle, through the C ABI."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from helpers import assert_close_to_oracle
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pv():
+    import packed_varlen_gb300 as pv
+    pv.load_library()
+    pv.get_device_status()
+    return pv
+
+
+def _run(pv, w, lb, la):
+    q, k, v = w.q.cuda(), w.k.cuda(), w.v.cuda()
+    out = pv.block_window_attn_fwd(q, k, v, w.block, lb, la, scale=w.scale)
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+LOOKS = [(0, 0), (1, 0), (0, 1), (1, 1), (2, 3)]
+
+
+@pytest.mark.parametrize("n", [10, 24, 96, 101])
+@pytest.mark.parametrize("look", LOOKS)
+def test_pages_unit_cases(pv, n, look):
+    # shorter than a block, exactly one block, whole blocks, a partial last block
+    w = workloads.random_block_window(1, n, 4, 64, 24, seed=n + 10 * look[0] + look[1])
+    got = oracle.to_f64(_run(pv, w, *look))
+    want = oracle.block_window_attention(w.q, w.k, w.v, 24, look[0], look[1], w.scale)
+    assert_close_to_oracle(got, want, f"n={n} look={look}")
+
+
+@pytest.mark.parametrize("n", [2400, 2390])
+@pytest.mark.parametrize("look", [(0, 0), (1, 1)])
+def test_token2wav_config(pv, n, look):
+    w = workloads.token2wav(n=n)
+    got = oracle.to_f64(_run(pv, w, *look))
+    want = oracle.block_window_attention(w.q, w.k, w.v, w.block, look[0], look[1], w.scale)
+    assert_close_to_oracle(got, want, f"token2wav n={n} look={look}")
+    assert pv.get_device_status() == 0
+
+
+@pytest.mark.parametrize("block,D", [(1, 64), (7, 128), (64, 64), (200, 128)])
+def test_other_blocks_and_head_dims(pv, block, D):
+    w = workloads.random_block_window(2, 333, 3, D, block, seed=block + D)
+    for lb, la in [(0, 0), (1, 2)]:
+        got = oracle.to_f64(_run(pv, w, lb, la))
+        want = oracle.block_window_attention(w.q, w.k, w.v, block, lb, la, w.scale)
+        assert_close_to_oracle(got, want, f"block={block} D={D} look=({lb},{la})")
+
+
+def test_block_one_returns_values(pv):
+    # block 1, no neighbours: every query sees only its own key, out = v
+    w = workloads.random_block_window(1, 77, 2, 64, 1, seed=5)
+    got = _run(pv, w, 0, 0)
+    assert torch.equal(got.view(torch.int16), w.v.view(torch.int16))
+
+
+def test_window_keys_outside_do_not_matter(pv):
+    w = workloads.random_block_window(1, 96, 2, 64, 24, seed=6)
+    base = _run(pv, w, 1, 0)
+    k2, v2 = w.k.clone(), w.v.clone()
+    k2[0, 48:] = 100.0
+    v2[0, 48:] = -100.0
+    w2 = workloads.BlockWindowWorkload("p", 1, 96, 2, 64, 24, [(1, 0)], w.q, k2, v2, 6)
+    pert = _run(pv, w2, 1, 0)
+    assert torch.equal(base[0, :48].view(torch.int16), pert[0, :48].view(torch.int16))

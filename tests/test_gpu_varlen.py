@@ -1,0 +1,162 @@
+"""Parity of the CUDA varlen attention path with the fp64 oracle, through the
+C ABI, plus the packed-vs-alone bit identity the pages require."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+from helpers import assert_close_to_oracle, gpu_varlen, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def pv():
+    import packed_varlen_gb300 as pv
+    pv.load_library()
+    pv.get_device_status()  # clear any earlier record
+    return pv
+
+
+def _check_full(pv, w, what):
+    out, cu_q, cu_k = gpu_varlen(pv, w)
+    ocq = oracle.cu_seqlens_from_lengths(w.lengths_q)
+    ock = oracle.cu_seqlens_from_lengths(w.lengths_k)
+    assert np.array_equal(cu_q.numpy(), ocq) and np.array_equal(cu_k.numpy(), ock)
+    want = oracle.varlen_attention(w.q, w.k, w.v, ocq, ock, w.scale)
+    T = int(ocq[-1])
+    got = oracle.to_f64(out)
+    assert_close_to_oracle(got[:T], want[:T], what)
+    assert np.isnan(got[T:]).all(), "rows outside every sequence were written"
+    assert pv.get_device_status() == 0
+
+
+def test_tiny_config(pv):
+    _check_full(pv, workloads.tiny(), "tiny")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("lengths", [
+    [1], [127], [128], [129], [300, 17, 256, 1],        # tails around the 128-row tile
+    [0, 200, 0, 5],                                      # empty sequences
+    [513, 1000],                                         # several tiles, ragged
+])
+def test_random_self_attention(pv, D, lengths):
+    w = workloads.random_varlen(lengths, None, 3, D, seed=sum(lengths) + D)
+    _check_full(pv, w, f"L={lengths} D={D}")
+
+
+@pytest.mark.parametrize("lq,lk", [([5, 300, 128], [400, 7, 128]), ([200, 3], [0, 260])])
+def test_cross_lengths_and_empty_keys(pv, lq, lk):
+    w = workloads.random_varlen(lq, lk, 2, 128, seed=99)
+    _check_full(pv, w, f"Lq={lq} Lk={lk}")
+
+
+def test_many_sequences(pv):
+    rng = np.random.default_rng(7)
+    L = rng.integers(0, 200, size=300).tolist()
+    w = workloads.random_varlen(L, None, 2, 64, seed=8)
+    _check_full(pv, w, "300 sequences")
+
+
+def test_max_batch(pv):
+    L = ([1, 2, 0, 130] * 256)[:1024]
+    w = workloads.random_varlen(L, None, 1, 64, seed=9)
+    _check_full(pv, w, "1024 sequences")
+
+
+def test_scale_argument(pv):
+    w = workloads.random_varlen([150, 40], None, 2, 128, seed=11)
+    for scale in (0.0, 0.02, 0.3):
+        out, _, _ = gpu_varlen(pv, w, scale=scale)
+        cu = oracle.cu_seqlens_from_lengths(w.lengths_q)
+        want = oracle.varlen_attention(w.q, w.k, w.v, cu, cu, scale)
+        assert_close_to_oracle(oracle.to_f64(out), want, f"scale={scale}")
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("name", ["mixed_res_mmdit", "single_edit", "cfg_dynamic_batch"])
+def test_full_size_configs_sampled(pv, name):
+    w = workloads.VARLEN_CONFIGS[name]()
+    out, cu_q, _ = gpu_varlen(pv, w)
+    rows = sample_rows(w.lengths_q, per_seq=8, seed=1)
+    cu = oracle.cu_seqlens_from_lengths(w.lengths_q)
+    want = oracle.varlen_attention(w.q, w.k, w.v, cu, cu, w.scale, rows=rows)
+    assert_close_to_oracle(oracle.to_f64(out[rows]), want, name)
+    assert pv.get_device_status() == 0
+
+
+@pytest.mark.slow
+def test_padded_tail_equals_masked_oracle(pv):
+    # 7 auto-padded rows after the edit request: trimmed by cu_seqlens, never
+    # read as keys, never written; equal to the key-padding-masked oracle
+    w = workloads.single_edit(pad_rows=7)
+    T = sum(w.lengths_q)
+    out, _, _ = gpu_varlen(pv, w)
+    assert out.shape[0] == T + 7
+    assert torch.isnan(out[T:].float()).all()
+    rows = sample_rows(w.lengths_q, per_seq=8, seed=2)
+    want = oracle.key_padding_attention(w.q, w.k, w.v, T, w.scale, rows=rows)
+    assert_close_to_oracle(oracle.to_f64(out[rows]), want, "padded tail")
+
+
+def _alone(pv, w, b):
+    s0, s1 = sum(w.lengths_q[:b]), sum(w.lengths_q[:b + 1])
+    k0, k1 = sum(w.lengths_k[:b]), sum(w.lengths_k[:b + 1])
+    one = workloads.VarlenWorkload("one", [w.lengths_q[b]], [w.lengths_k[b]], w.H, w.D,
+                                   w.q[s0:s1].clone(), w.k[k0:k1].clone(), w.v[k0:k1].clone(),
+                                   w.seed)
+    out, _, _ = gpu_varlen(pv, one)
+    return out
+
+
+@pytest.mark.parametrize("name", ["mixed_res_mmdit", "small"])
+def test_packed_bit_identical_to_alone(pv, name):
+    if name == "small":
+        w = workloads.random_varlen([300, 1, 129, 64, 700], None, 4, 128, seed=12)
+    else:
+        w = workloads.mixed_res()
+    packed, _, _ = gpu_varlen(pv, w)
+    start = 0
+    for b, L in enumerate(w.lengths_q):
+        alone = _alone(pv, w, b)
+        assert torch.equal(packed[start:start + L].view(torch.int16), alone.view(torch.int16)), \
+            f"sequence {b} differs packed vs alone"
+        start += L
+
+
+def test_request_permutation_bit_identical(pv):
+    w = workloads.random_varlen([200, 333, 64, 129], None, 2, 128, seed=13)
+    base, _, _ = gpu_varlen(pv, w)
+    perm = [3, 1, 0, 2]
+    cu = [0]
+    for L in w.lengths_q:
+        cu.append(cu[-1] + L)
+    segs = [slice(cu[b], cu[b + 1]) for b in perm]
+    wp = workloads.VarlenWorkload("perm", [w.lengths_q[b] for b in perm],
+                                  [w.lengths_k[b] for b in perm], w.H, w.D,
+                                  torch.cat([w.q[s] for s in segs]),
+                                  torch.cat([w.k[s] for s in segs]),
+                                  torch.cat([w.v[s] for s in segs]), w.seed)
+    got, _, _ = gpu_varlen(pv, wp)
+    want = torch.cat([base[s] for s in segs])
+    assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+
+
+def test_device_checks_record_errors(pv):
+    dev = "cuda"
+    q = torch.randn(64, 2, 64, device=dev).to(torch.bfloat16)
+    out = torch.full_like(q, 3.0)
+    bad = torch.tensor([0, 40, 30], dtype=torch.int32, device=dev)   # decreasing
+    pv.varlen_attn_fwd(q, q, q, bad, bad, 64, 64, out=out)
+    assert pv.get_device_status() == 1
+    assert (out[40:].float() == 3.0).all()   # the bad sequence was skipped
+    assert (out[:40].float() != 3.0).any()   # the good one was not
+    out.fill_(3.0)
+    ok = torch.tensor([0, 40, 64], dtype=torch.int32, device=dev)
+    pv.varlen_attn_fwd(q, q, q, ok, ok, 30, 64, out=out)              # 40 > max_q
+    assert pv.get_device_status() == 2
+    assert (out[:40].float() == 3.0).all()
+    assert (out[40:].float() != 3.0).any()
+    assert pv.get_device_status() == 0      # cleared by the read
