@@ -1,7 +1,8 @@
-// Block-window attention (Token2Wav DiT) and the first varlen attention path:
-// register-tiled flash attention on warp-level mma.sync (bf16 in, fp32
-// accumulate), cp.async double-buffered K/V tiles in swizzled shared memory,
-// online softmax in fp32 with quad shuffles.
+// Block-window attention (Token2Wav DiT): register-tiled flash attention on
+// warp-level mma.sync (bf16 in, fp32 accumulate), cp.async double-buffered
+// K/V tiles in swizzled shared memory, online softmax in fp32 with quad
+// shuffles.  The windows are short (24-72 keys per query) and the layer is
+// bound by HBM traffic and launch latency, not by the tensor pipe.
 //
 // Block window: "[Perf][Model] Use block-sparse attention in Qwen2.5-Omni
 // Token2Wav DiT" (Change).  A CTA owns 64 query rows; it visits only the key
@@ -318,27 +319,6 @@ cudaError_t launch_block_window_attn(const BlockWindowArgs &a, cudaStream_t stre
   p.status = a.status;
   dim3 grid((a.n + kBr - 1) / kBr, a.H, a.batch);
   return a.D == 64 ? launch_mma<64, true>(p, grid, stream) : launch_mma<128, true>(p, grid, stream);
-}
-
-cudaError_t launch_varlen_attn(const VarlenArgs &a, cudaStream_t stream) {
-  MmaParams p{};
-  p.q = static_cast<const __nv_bfloat16 *>(a.q);
-  p.k = static_cast<const __nv_bfloat16 *>(a.k);
-  p.v = static_cast<const __nv_bfloat16 *>(a.v);
-  p.out = static_cast<__nv_bfloat16 *>(a.out);
-  p.row_stride = static_cast<int64_t>(a.H) * a.D;
-  p.scale_log2 = a.scale * 1.4426950408889634f;
-  p.H = a.H;
-  p.cu_q = a.cu_q;
-  p.cu_k = a.cu_k;
-  p.total_q = a.total_q;
-  p.total_k = a.total_k;
-  p.max_q = a.max_q;
-  p.max_k = a.max_k;
-  p.status = a.status;
-  if (a.max_q == 0) return cudaSuccess;
-  dim3 grid((a.max_q + kBr - 1) / kBr, a.H, a.batch);
-  return a.D == 64 ? launch_mma<64, false>(p, grid, stream) : launch_mma<128, false>(p, grid, stream);
 }
 
 }  // namespace pa
