@@ -106,6 +106,21 @@ def _profiled_traffic(digest: str):
     return None
 
 
+def rank_seed(rank: int, base: int = 1002) -> int:
+    """Value seed of the batch a rank processes: every rank holds its own batch
+    of the same shape (same lengths, weak scaling); no data moves between ranks."""
+    return base + 7919 * rank
+
+
+def max_over_ranks(value: float, dist=None, device=None) -> float:
+    """The slowest rank's time: the job finishes when its last rank does."""
+    if dist is None or not dist.is_initialized() or dist.get_world_size() == 1:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
 class ClockSampler:
     """nvidia-smi clock/throttle samples taken while the timed region runs."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -239,7 +254,7 @@ def run_ours(args):
     pv.get_device_status()
 
     # ---- inputs: this rank's padded batch, resident in HBM -------------------
-    pw = workloads.mixed_res_padded(seed=2 + 1000 * rank)
+    pw = workloads.mixed_res_padded(seed=2, value_seed=rank_seed(rank))
     L = pw.lengths
     T, H, D, B, S = sum(L), pw.H, pw.D, len(L), pw.s_max
     flops = 4 * H * D * sum(x * x for x in L)
@@ -298,11 +313,7 @@ def run_ours(args):
     clocks = sampler.stop()
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
     attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
-    total_ms = sum(step_ms)
-    if dist:
-        t = torch.tensor([total_ms], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(sum(step_ms), dist, dev)
     value = flops * ws * args.steps / (total_ms * 1e-3) / 1e12
 
     # ---- end to end: host buffers in, host result out ----------------------
@@ -332,13 +343,7 @@ def run_ours(args):
         e1.record(stream)
         torch.cuda.synchronize()
         e2e_ms.append(e0.elapsed_time(e1))
-    e2e_total = sum(e2e_ms)
-    if dist:
-        t = torch.tensor([e2e_total / len(e2e_ms)], device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_mean = float(t.item())
-    else:
-        e2e_mean = e2e_total / len(e2e_ms)
+    e2e_mean = max_over_ranks(sum(e2e_ms) / len(e2e_ms), dist, dev)
     e2e_value = flops * ws / (e2e_mean * 1e-3) / 1e12
 
     # ---- block-window variant (Token2Wav), timed per layer -------------------
@@ -422,6 +427,45 @@ def run_ours(args):
     return 0
 
 
+def run_attn_only(args):
+    """Attention kernel alone on one workload (for profiling runs): W + K
+    launches on resident inputs, L2 flushed between launches."""
+    import packed_varlen_gb300 as pv
+    torch.cuda.set_device(0)
+    dev = torch.device("cuda", 0)
+    pv.load_library()
+    pv.get_device_status()
+    if args.workload in workloads.VARLEN_CONFIGS:
+        w = workloads.VARLEN_CONFIGS[args.workload]()
+    else:
+        n = int(args.workload.split("_")[-1].rstrip("k")) * 1024
+        w = workloads.random_varlen([n], None, 24, 128, seed=n, name=args.workload)
+    q, k, v = w.q.to(dev), w.k.to(dev), w.v.to(dev)
+    cu = pv.cu_seqlens_from_lengths(torch.tensor(w.lengths_q, dtype=torch.int32, device=dev))
+    out = torch.empty_like(q)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flops = 4 * w.H * w.D * sum(a * b for a, b in zip(w.lengths_q, w.lengths_k))
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        pv.varlen_attn_fwd(q, k, v, cu, cu, max(w.lengths_q), max(w.lengths_k), out=out)
+    torch.cuda.synchronize()
+    ts = []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        pv.varlen_attn_fwd(q, k, v, cu, cu, max(w.lengths_q), max(w.lengths_k), out=out)
+        e1.record(stream)
+        ts.append((e0, e1))
+    torch.cuda.synchronize()
+    if pv.get_device_status() != 0:
+        raise RuntimeError("device status error")
+    ms = statistics.median(a.elapsed_time(b) for a, b in ts)
+    print(json.dumps({"workload": w.name, "lengths": w.lengths_q, "H": w.H, "D": w.D,
+                      "attn_ms": ms, "tflops": flops / (ms * 1e-3) / 1e12}), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -433,7 +477,13 @@ def main():
     ap.add_argument("--ref-rows", type=int, default=128,
                     help="query rows per sequence per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--attn-only", action="store_true",
+                    help="time the attention kernel alone (profiling); not the bench line")
+    ap.add_argument("--workload", default="single_8k",
+                    help="with --attn-only: a varlen config name or single_<N>k")
     args = ap.parse_args()
+    if args.attn_only:
+        return run_attn_only(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

@@ -187,6 +187,16 @@ pa_status pa_varlen_work_order(const int32_t *cu_seqlens_q, const int32_t *cu_se
  */
 pa_status pa_get_device_status(int32_t *code);
 
+/*
+ * pa_selftest_wait_timeout -- exercises the bounded-wait path the pipelined
+ * kernels use: one CTA waits on an mbarrier that nothing ever arrives at,
+ * gives up after about `timeout_us` microseconds (1 .. 10,000,000), records
+ * PA_DEVICE_ERR_TIMEOUT in the status word and returns, leaving the context
+ * usable.  No counterpart on the pages; it tests this library's own failure
+ * handling without faulting the GPU.
+ */
+pa_status pa_selftest_wait_timeout(int32_t timeout_us, pa_stream_t stream);
+
 /* Human-readable name of a status code (static string, never NULL). */
 const char *pa_status_string(pa_status status);
 

@@ -53,6 +53,7 @@ _SIGNATURES = {
                              _c_i32),
     "pa_get_device_status": ([ctypes.POINTER(_c_i32)], _c_i32),
     "pa_status_string": ([_c_i32], ctypes.c_char_p),
+    "pa_selftest_wait_timeout": ([_c_i32, _c_ptr], _c_i32),
 }
 
 
@@ -254,6 +255,13 @@ def get_device_status() -> int:
     if st not in (PA_OK, 5):
         raise PackedAttnError("pa_get_device_status", st)
     return int(code.value)
+
+
+def selftest_wait_timeout(timeout_us: int = 1000, stream=None) -> None:
+    """Launch the bounded-wait self-test (pa_selftest_wait_timeout)."""
+    lib = load_library()
+    _check("pa_selftest_wait_timeout",
+           lib.pa_selftest_wait_timeout(int(timeout_us), _stream(stream)))
 
 
 def status_string(status: int) -> str:

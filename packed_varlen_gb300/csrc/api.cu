@@ -7,6 +7,7 @@
 
 #include "internal.h"
 #include "sched.cuh"
+#include "tc_ptx.cuh"
 
 namespace pa {
 namespace {
@@ -151,6 +152,23 @@ __global__ void __launch_bounds__(kOrderThreads)
   }
 }
 
+// One CTA waits on an mbarrier nothing arrives at, through the same bounded
+// wait the pipelined kernels use, and must come back with a timeout record.
+__global__ void wait_timeout_kernel(long long limit_cycles, int32_t *status) {
+  __shared__ __align__(8) uint64_t bar;
+  __shared__ int32_t abort_flag;
+  const uint32_t b = tc::smem_u32(&bar);
+  if (threadIdx.x == 0) {
+    tc::mbar_init(b, 1);
+    abort_flag = 0;
+    tc::fence_mbar_init();
+  }
+  __syncthreads();
+  if (threadIdx.x == 0)
+    tc::bounded_wait(b, 0, reinterpret_cast<volatile int32_t *>(&abort_flag), status,
+                     limit_cycles);
+}
+
 pa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
 
 }  // namespace
@@ -288,6 +306,21 @@ pa_status pa_varlen_work_order(const int32_t *cu_q, const int32_t *cu_k, int32_t
   const size_t smem = sizeof(int32_t) * (4 * static_cast<size_t>(batch) + 1);
   work_order_kernel<<<1, kOrderThreads, smem, reinterpret_cast<cudaStream_t>(stream)>>>(
       cu_q, cu_k, batch, H, tile_m, items, capacity, status);
+  return from_cuda(cudaGetLastError());
+}
+
+pa_status pa_selftest_wait_timeout(int32_t timeout_us, pa_stream_t stream) {
+  if (timeout_us < 1 || timeout_us > 10000000) return PA_ERR_INVALID_ARG;
+  int32_t *status;
+  int sms;
+  if (device_context(&status, &sms) != cudaSuccess) return PA_ERR_CUDA;
+  int dev = 0, khz = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&khz, cudaDevAttrClockRate, dev) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (khz <= 0) khz = 2000000;
+  const long long cycles = static_cast<long long>(timeout_us) * khz / 1000;
+  wait_timeout_kernel<<<1, 32, 0, reinterpret_cast<cudaStream_t>(stream)>>>(cycles, status);
   return from_cuda(cudaGetLastError());
 }
 

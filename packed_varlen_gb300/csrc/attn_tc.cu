@@ -279,6 +279,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int row = quad * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     const float sl2 = p.scale_log2;
+    const bool pos_scale = sl2 > 0.f;
+    const float mul = pos_scale ? sl2 : 1.f;
     uint32_t g = 0;
     bool ok = true;
     for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
@@ -303,28 +305,42 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         fence_after_sync();
-        float x[kTile];
-        {
-          uint32_t r[32];
+        // all four 32-column loads in flight, then one wait
+        uint32_t sr[kTile];
 #pragma unroll
-          for (int c = 0; c < kTile / 32; ++c) {
-            tmem_ld32(lane_base + C::kColS + buf * kTile + c * 32, r);
-            tmem_wait_ld();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) x[c * 32 + e] = __uint_as_float(r[e]) * sl2;
-          }
-        }
+        for (int c = 0; c < kTile / 32; ++c)
+          tmem_ld32(lane_base + C::kColS + buf * kTile + c * 32,
+                    *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+        tmem_wait_ld();
         fence_before_sync();
         mbar_arrive(bar(C::kSFree + buf));
+        // x = raw scores as pairs; with a positive scale the scale is folded
+        // into the exponent's FFMA, otherwise the scores are scaled first
+        float2 x[kTile / 2];
+#pragma unroll
+        for (int c = 0; c < kTile / 2; ++c)
+          x[c] = make_float2(__uint_as_float(sr[2 * c]), __uint_as_float(sr[2 * c + 1]));
+        if (!pos_scale) {
+          const float2 s2 = make_float2(sl2, sl2);
+#pragma unroll
+          for (int c = 0; c < kTile / 2; ++c) x[c] = __fmul2_rn(x[c], s2);
+        }
         if (j == it.nk - 1) {
           const int valid = it.lk - j * kTile;
 #pragma unroll
-          for (int c = 0; c < kTile; ++c)
-            if (c >= valid) x[c] = -INFINITY;
+          for (int c = 0; c < kTile / 2; ++c) {
+            if (2 * c >= valid) x[c].x = -INFINITY;
+            if (2 * c + 1 >= valid) x[c].y = -INFINITY;
+          }
         }
-        float mx = x[0];
+        // row maximum: eight independent chains of 3-input max, fixed combine
+        float mx8[8];
 #pragma unroll
-        for (int c = 1; c < kTile; ++c) mx = fmaxf(mx, x[c]);
+        for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(x[e].x, x[e].y);
+#pragma unroll
+        for (int c = 8; c < kTile / 2; ++c) mx8[c & 7] = fmax3(mx8[c & 7], x[c].x, x[c].y);
+        const float mx = fmax3(fmax3(mx8[0], mx8[1], mx8[2]), fmax3(mx8[3], mx8[4], mx8[5]),
+                               fmaxf(mx8[6], mx8[7])) * mul;
         float alpha = 1.f;
         bool rescale = false;
         if (j == 0) {
@@ -334,14 +350,22 @@ __global__ void __launch_bounds__(kThreads, 1)
           m = mx;
           rescale = true;
         }
-        float sum = 0.f;
+        const float2 mul2 = make_float2(mul, mul), negm2 = make_float2(-m, -m);
+        float2 sum8[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) sum8[e] = make_float2(0.f, 0.f);
         uint32_t pk[kTile / 2];
 #pragma unroll
-        for (int c = 0; c < kTile; c += 2) {
-          const float p0 = ex2(x[c] - m), p1 = ex2(x[c + 1] - m);
-          sum += p0 + p1;
-          pk[c / 2] = pack_bf16x2(p0, p1);
+        for (int c = 0; c < kTile / 2; ++c) {
+          const float2 t = __ffma2_rn(x[c], mul2, negm2);
+          const float2 pp = make_float2(ex2(t.x), ex2(t.y));
+          sum8[c & 7] = __fadd2_rn(sum8[c & 7], pp);
+          pk[c] = pack_bf16x2(pp.x, pp.y);
         }
+        const float2 s01 = __fadd2_rn(__fadd2_rn(sum8[0], sum8[1]), __fadd2_rn(sum8[2], sum8[3]));
+        const float2 s45 = __fadd2_rn(__fadd2_rn(sum8[4], sum8[5]), __fadd2_rn(sum8[6], sum8[7]));
+        const float2 s8 = __fadd2_rn(s01, s45);
+        const float sum = s8.x + s8.y;
         l = l * alpha + sum;
         if (j >= 1) {
           // PV of the previous tile must be done: it updates O and reads P

@@ -207,11 +207,14 @@ def padded(lengths: List[int], H: int, D: int, seed: int,
     return PaddedWorkload(name, list(lengths), s, H, D, q, k, v, seed)
 
 
-def mixed_res_padded(seed: int = 2) -> PaddedWorkload:
-    """The mixed-resolution batch in the padded layout the pack step reads."""
+def mixed_res_padded(seed: int = 2, value_seed: Optional[int] = None) -> PaddedWorkload:
+    """The mixed-resolution batch in the padded layout the pack step reads.
+    Lengths come from ``seed``; values from ``value_seed`` (default seed + 1000),
+    so several ranks can hold batches of one shape with different values."""
     g = torch.Generator().manual_seed(seed)
     L = lengths_mixed_res(g)
-    return padded(L, 24, 128, seed + 1000, name="mixed_res_mmdit_padded")
+    vs = seed + 1000 if value_seed is None else value_seed
+    return padded(L, 24, 128, vs, name="mixed_res_mmdit_padded")
 
 
 def random_varlen(lengths_q: List[int], lengths_k: Optional[List[int]], H: int, D: int,
