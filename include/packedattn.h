@@ -56,8 +56,8 @@ typedef enum {
 /* Largest batch (number of packed sequences) the attention kernels accept. */
 #define PA_MAX_BATCH 1024
 
-/* Query rows per work item of pa_varlen_attn_fwd. */
-#define PA_VARLEN_TILE_M 128
+/* Query rows per work item of pa_varlen_attn_fwd (two 128-row tensor-core tiles). */
+#define PA_VARLEN_TILE_M 256
 
 /*
  * pa_varlen_attn_fwd -- non-causal softmax attention over a flat packed batch.
@@ -196,6 +196,10 @@ pa_status pa_get_device_status(int32_t *code);
  * handling without faulting the GPU.
  */
 pa_status pa_selftest_wait_timeout(int32_t timeout_us, pa_stream_t stream);
+
+/* Name of the last CUDA error this thread met inside the library, the cause
+ * behind a PA_ERR_CUDA (static string, never NULL; "cudaSuccess" if none). */
+const char *pa_last_cuda_error(void);
 
 /* Human-readable name of a status code (static string, never NULL). */
 const char *pa_status_string(pa_status status);

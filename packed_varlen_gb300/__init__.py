@@ -26,12 +26,13 @@ DEVICE_ERRORS = {0: "PA_DEVICE_OK", 1: "PA_DEVICE_ERR_CU_SEQLENS", 2: "PA_DEVICE
                  3: "PA_DEVICE_ERR_TIMEOUT", 4: "PA_DEVICE_ERR_LENGTH",
                  5: "PA_DEVICE_ERR_CAPACITY"}
 MAX_BATCH = 1024
-VARLEN_TILE_M = 128
+VARLEN_TILE_M = 256
 
 
 class PackedAttnError(RuntimeError):
-    def __init__(self, fn: str, status: int):
-        super().__init__(f"{fn} returned {STATUS_NAMES.get(status, status)}")
+    def __init__(self, fn: str, status: int, detail: str = ""):
+        msg = f"{fn} returned {STATUS_NAMES.get(status, status)}"
+        super().__init__(msg + (f" ({detail})" if detail else ""))
         self.status = status
 
 
@@ -54,6 +55,7 @@ _SIGNATURES = {
     "pa_get_device_status": ([ctypes.POINTER(_c_i32)], _c_i32),
     "pa_status_string": ([_c_i32], ctypes.c_char_p),
     "pa_selftest_wait_timeout": ([_c_i32, _c_ptr], _c_i32),
+    "pa_last_cuda_error": ([], ctypes.c_char_p),
 }
 
 
@@ -80,7 +82,10 @@ def load_library(path: Optional[str] = None) -> ctypes.CDLL:
 
 def _check(fn: str, status: int):
     if status != PA_OK:
-        raise PackedAttnError(fn, status)
+        detail = ""
+        if status == 4 and _lib is not None:
+            detail = _lib.pa_last_cuda_error().decode()
+        raise PackedAttnError(fn, status, detail)
 
 
 def _stream(stream) -> int:

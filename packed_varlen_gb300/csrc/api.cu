@@ -169,7 +169,14 @@ __global__ void wait_timeout_kernel(long long limit_cycles, int32_t *status) {
                      limit_cycles);
 }
 
-pa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CUDA; }
+// Last CUDA error this thread saw inside the library (for pa_last_cuda_error).
+thread_local cudaError_t t_last_cuda_error = cudaSuccess;
+
+pa_status from_cuda(cudaError_t e) {
+  if (e == cudaSuccess) return PA_OK;
+  t_last_cuda_error = e;
+  return PA_ERR_CUDA;
+}
 
 }  // namespace
 }  // namespace pa
@@ -177,6 +184,8 @@ pa_status from_cuda(cudaError_t e) { return e == cudaSuccess ? PA_OK : PA_ERR_CU
 using namespace pa;
 
 extern "C" {
+
+const char *pa_last_cuda_error(void) { return cudaGetErrorName(t_last_cuda_error); }
 
 const char *pa_status_string(pa_status s) {
   switch (s) {
@@ -207,7 +216,7 @@ pa_status pa_varlen_attn_fwd(const void *q, const void *k, const void *v, void *
   VarlenArgs a{q, k, v, out, cu_seqlens_q, cu_seqlens_k, batch, total_q, total_k, max_q,
                max_k, H, D, scale, nullptr, 0};
   cudaError_t e = device_context(&a.status, &a.num_sms);
-  if (e != cudaSuccess) return PA_ERR_CUDA;
+  if (e != cudaSuccess) return from_cuda(e);
   return from_cuda(launch_varlen_attn(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 
@@ -225,7 +234,7 @@ pa_status pa_block_window_attn_fwd(const void *q, const void *k, const void *v, 
   BlockWindowArgs a{q, k, v, out, batch, n, block, look_back, look_ahead, H, D, scale,
                     nullptr, 0};
   cudaError_t e = device_context(&a.status, &a.num_sms);
-  if (e != cudaSuccess) return PA_ERR_CUDA;
+  if (e != cudaSuccess) return from_cuda(e);
   return from_cuda(launch_block_window_attn(a, reinterpret_cast<cudaStream_t>(stream)));
 }
 

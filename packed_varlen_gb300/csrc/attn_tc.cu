@@ -6,23 +6,31 @@
 // varlen attention for mixfusion", Key changes; "feat: Support dynamic
 // batching for heterogeneous diffusion requests", AttentionMetadata).
 //
-// Design (one persistent CTA per SM, 6 warps):
-//   warp 0      TMA producer: Q tile once per work item, then K/V tiles in
-//               the order the MMAs consume them (K0, K1, V0, K2, V1, ...)
+// Design: one persistent CTA per SM, 10 warps.  A work item is 256 query
+// rows of one (sequence, head), held as two 128-row tiles Q0 and Q1 that share
+// every K/V tile loaded, so each K/V byte brought into shared memory feeds
+// twice the tensor-core work of a single-tile item.
+//   warp 0      TMA producer: Q0/Q1 once per item, then K0, V0, K1, V1, ...
 //               through a ring of shared-memory slots.
-//   warp 1      allocates TMEM; lane 0 issues tcgen05.mma:
-//               S = Q K^T (A, B from shared memory, fp32 into TMEM, double
-//               buffered) and O += P V (P from TMEM as bf16, V from shared
-//               memory, fp32 accumulator in TMEM).
-//   warps 2..5  one thread per query row: read S from TMEM, online softmax
-//               in fp32 (exp2 with the scale folded in), write P to TMEM,
-//               rescale O in TMEM only when the row maximum grew by more
-//               than 2^8, and finally normalise O and store bf16 rows.
-// Work items (sequence, head, 128-row query tile) come from the
-// length-ordered list of sched.cuh; every item is computed by one CTA in a
-// fixed key-tile order, so results do not depend on the rest of the batch.
-// Key columns past the sequence end are masked to -inf (P = 0 there); query
-// rows past it are computed but never stored.  Every mbarrier wait is bounded.
+//   warp 1      allocates TMEM (S0, S1, O0, O1: 128 columns each); lane 0
+//               issues tcgen05.mma in the order
+//                 S0_0 S1_0 | PV0_0 S0_1 PV1_0 S1_1 | PV0_1 S0_2 ...
+//               S = Q K^T with both operands in shared memory, fp32 into TMEM;
+//               O += P V with P (bf16) read from TMEM, V from shared memory.
+//               While one tile's softmax runs, the tensor core computes the
+//               other tile's PV and next S.
+//   warps 2..5  softmax of tile 0, one thread per query row (TMEM lane);
+//   warps 6..9  softmax of tile 1.  Each thread reads its row of S, runs the
+//               online softmax in fp32 (exp2 with the scale folded in),
+//               writes P as bf16 over the first 64 columns of its S buffer,
+//               rescales O in TMEM only when the row maximum grew by more
+//               than 2^8, and finally normalises O and stores bf16 rows.
+// P overwrites S in place: the MMA that next writes that S buffer is issued
+// after the PV that reads P, and tcgen05 MMAs of one CTA execute in order.
+// Every output row is computed by one CTA in a fixed key-tile order that
+// depends only on its own sequence, so results do not depend on the rest of
+// the batch.  Key columns past the sequence end are masked to -inf (P = 0);
+// query rows past it are computed but never stored.  Every wait is bounded.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -37,8 +45,9 @@ namespace {
 
 using namespace tc;
 
-constexpr int kTile = 128;          // query rows per item and keys per tile
-constexpr int kThreads = 192;       // 6 warps
+constexpr int kTile = 128;          // rows of a Q tile, keys of a K/V tile
+constexpr int kItemRows = 256;      // query rows per work item (two tiles)
+constexpr int kThreads = 320;       // producer, MMA, 2 x 4 softmax warps
 constexpr long long kWaitLimit = 4000000000LL;  // clock cycles (~2 s)
 constexpr long long kDrainLimit = 400000000LL;  // teardown after an abort (~0.2 s)
 constexpr float kRescaleThreshold = 8.0f;       // log2 units
@@ -47,21 +56,20 @@ template <int D>
 struct Cfg {
   static constexpr int kHalfBytes = kTile * 64 * 2;         // 128 rows x 128 B
   static constexpr int kTileBytes = kTile * D * 2;          // one Q/K/V tile
-  static constexpr int kSlots = D == 128 ? 5 : 10;
-  static constexpr int kQOff = 0;
-  static constexpr int kRingOff = kTileBytes;
+  static constexpr int kSlots = D == 128 ? 4 : 8;
+  static constexpr int kQOff = 0;                           // Q0, Q1
+  static constexpr int kRingOff = 2 * kTileBytes;
   static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
-  // barrier indices
-  static constexpr int kQFull = 0, kQEmpty = 1, kSFull = 2, kSFree = 4, kPReady = 6,
-                       kPVDone = 7, kFinal = 8, kSlotFull = 9, kSlotEmpty = 9 + kSlots;
+  // barriers: per Q tile t an S-full, a P-ready and an O-full barrier
+  static constexpr int kQFull = 0, kQEmpty = 1, kSFull = 2, kPReady = 4, kOFull = 6,
+                       kFinal = 8, kSlotFull = 9, kSlotEmpty = 9 + kSlots;
   static constexpr int kNumBars = 9 + 2 * kSlots;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;   // tmem base, abort flag
   static constexpr int kSchedOff = (kMiscOff + 16 + 127) / 128 * 128;
   static constexpr int kSmemBytes = kSchedOff + (2 * PA_MAX_BATCH + 1) * 4 + 1024;
-  // TMEM columns
-  static constexpr uint32_t kColS = 0;           // S buffers at 0 and 128
-  static constexpr uint32_t kColO = 256;         // O: D columns
-  static constexpr uint32_t kColP = 256 + D;     // P: 64 columns (128 bf16)
+  // TMEM columns: S_t at 128 t (P_t over its first 64), O_t at 256 + D t
+  static constexpr uint32_t kColS = 0;
+  static constexpr uint32_t kColO = 256;
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kIdescS = idesc_bf16_f32(kTile, kTile, false);
   static constexpr uint32_t kIdescO = idesc_bf16_f32(kTile, D, true);
@@ -79,13 +87,24 @@ struct TcParams {
 };
 
 struct ItemInfo {
-  int q_row0;   // global row of the tile's first query
-  int rows;     // valid query rows in the tile (1..128)
+  int q_row0;   // global row of the item's first query
+  int rows;     // valid query rows in the item (1..256)
   int k0;       // global row of the sequence's first key
   int lk;       // keys of the sequence
   int nk;       // key tiles
   int head;
+  int rot;      // first key tile visited
 };
+
+// Key tile visited j-th.  Items start at key tile (item index in the
+// sequence mod nk) and wrap around, so the CTAs of a wave, which hold
+// consecutive query blocks of one head, read different K/V tiles at any
+// moment.  The order depends only on the sequence's own lengths and the
+// item's position in it, so a sequence's result is the same in any batch.
+__device__ __forceinline__ int key_tile(const ItemInfo &it, int j) {
+  const int kt = it.rot + j;
+  return kt >= it.nk ? kt - it.nk : kt;
+}
 
 __device__ __forceinline__ ItemInfo item_info(const TcParams &p, const int32_t *order,
                                               const int32_t *prefix, int i) {
@@ -94,12 +113,13 @@ __device__ __forceinline__ ItemInfo item_info(const TcParams &p, const int32_t *
   const SeqBounds sb = seq_bounds(p.cu_q, p.cu_k, w.seq, p.total_q, p.total_k, p.max_q,
                                   p.max_k, err);
   ItemInfo it;
-  it.q_row0 = sb.q0 + w.tile * kTile;
-  it.rows = min(kTile, sb.lq - w.tile * kTile);
+  it.q_row0 = sb.q0 + w.tile * kItemRows;
+  it.rows = min(kItemRows, sb.lq - w.tile * kItemRows);
   it.k0 = sb.k0;
   it.lk = sb.lk;
   it.nk = (sb.lk + kTile - 1) / kTile;
   it.head = w.head;
+  it.rot = it.nk > 0 ? w.tile % it.nk : 0;
   return it;
 }
 
@@ -128,12 +148,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     mbar_init(bar(C::kQFull), 1);
     mbar_init(bar(C::kQEmpty), 1);
-    mbar_init(bar(C::kSFull + 0), 1);
-    mbar_init(bar(C::kSFull + 1), 1);
-    mbar_init(bar(C::kSFree + 0), 128);
-    mbar_init(bar(C::kSFree + 1), 128);
-    mbar_init(bar(C::kPReady), 128);
-    mbar_init(bar(C::kPVDone), 1);
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(bar(C::kSFull + t), 1);
+      mbar_init(bar(C::kPReady + t), 128);
+      mbar_init(bar(C::kOFull + t), 1);
+    }
     mbar_init(bar(C::kFinal), 1);
     for (int s = 0; s < C::kSlots; ++s) {
       mbar_init(bar(C::kSlotFull + s), 1);
@@ -145,8 +164,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_alloc(base + C::kMiscOff, C::kTmemCols);
   // the ring is free until the first load: use it for the build's temporaries
   int32_t *tmp = reinterpret_cast<int32_t *>(gbase + C::kRingOff);
-  sched_build(order, prefix, tmp, tmp + PA_MAX_BATCH, p.cu_q, p.cu_k, p.batch, p.H, kTile,
-              p.total_q, p.total_k, p.max_q, p.max_k, p.status, blockIdx.x == 0);
+  sched_build(order, prefix, tmp, tmp + PA_MAX_BATCH, p.cu_q, p.cu_k, p.batch, p.H,
+              kItemRows, p.total_q, p.total_k, p.max_q, p.max_k, p.status, blockIdx.x == 0);
   fence_before_sync();
   __syncthreads();
   fence_after_sync();
@@ -178,22 +197,25 @@ __global__ void __launch_bounds__(kThreads, 1)
       for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
         const ItemInfo it = item_info(p, order, prefix, i);
         if (it.nk == 0) continue;
+        const int ntq = it.rows > kTile ? 2 : 1;
         if (!bounded_wait(bar(C::kQEmpty), (q_loads & 1u) ^ 1u, abort_flag, p.status,
                           kWaitLimit)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(bar(C::kQFull), C::kTileBytes);
+        mbar_arrive_expect_tx(bar(C::kQFull), ntq * C::kTileBytes);
+        for (int t = 0; t < ntq; ++t) {
 #pragma unroll
-        for (int hf = 0; hf < D / 64; ++hf)
-          tma_load_3d(sQ + hf * C::kHalfBytes, &tm_q, bar(C::kQFull), hf * 64, it.head,
-                      it.q_row0);
+          for (int hf = 0; hf < D / 64; ++hf)
+            tma_load_3d(sQ + t * C::kTileBytes + hf * C::kHalfBytes, &tm_q, bar(C::kQFull),
+                        hf * 64, it.head, it.q_row0 + t * kTile);
+        }
         ++q_loads;
         for (int j = 0; j < it.nk && ok; ++j) {
-          ok = load_kv(&tm_k, it.k0 + j * kTile, it.head);
-          if (ok && j >= 1) ok = load_kv(&tm_v, it.k0 + (j - 1) * kTile, it.head);
+          const int row = it.k0 + key_tile(it, j) * kTile;
+          ok = load_kv(&tm_k, row, it.head);
+          if (ok) ok = load_kv(&tm_v, row, it.head);
         }
-        if (ok) ok = load_kv(&tm_v, it.k0 + (it.nk - 1) * kTile, it.head);
       }
       if (!ok) {
         // give the copies already issued a bounded chance to land
@@ -207,67 +229,104 @@ __global__ void __launch_bounds__(kThreads, 1)
   } else if (warp == 1) {
     // ================= MMA issuer =================
     if (lane == 0) {
-      uint32_t q_uses = 0, slot_uses = 0, g = 0;
+      uint32_t q_uses = 0, slot_uses = 0, issued = 0;
+      uint32_t p_waits[2] = {0, 0};
       bool ok = true;
-      // descriptors: Q/K K-major (SBO = 8 rows x 128 B), V MN-major
-      // (LBO = next 64-column half, SBO = next 8 keys)
-      auto issue_pv = [&](uint32_t gg, bool first) -> bool {
-        if (!bounded_wait(bar(C::kPReady), gg & 1u, abort_flag, p.status, kWaitLimit))
+      // next ring slot in consumption order, once its load has landed
+      auto wait_slot = [&](uint32_t &s) -> bool {
+        s = slot_uses % C::kSlots;
+        return bounded_wait(bar(C::kSlotFull + s), (slot_uses / C::kSlots) & 1u, abort_flag,
+                            p.status, kWaitLimit);
+      };
+      // S_t = Q_t K^T into S buffer t (Q/K K-major, SBO = 8 rows x 128 B)
+      auto issue_s = [&](int t, uint32_t k_addr) {
+#pragma unroll
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
+          const uint64_t adesc = sdesc_sw128(sQ + t * C::kTileBytes + off, 16, 1024);
+          const uint64_t bdesc = sdesc_sw128(k_addr + off, 16, 1024);
+          mma_ss(tmem + C::kColS + t * kTile, adesc, bdesc, C::kIdescS, kk > 0 ? 1u : 0u);
+        }
+        mma_commit(bar(C::kSFull + t));
+      };
+      // O_t += P_t V once tile t's softmax has written P_t
+      auto issue_pv = [&](int t, uint32_t v_addr, bool first) -> bool {
+        if (!bounded_wait(bar(C::kPReady + t), p_waits[t] & 1u, abort_flag, p.status,
+                          kWaitLimit))
           return false;
-        const uint32_t s = slot_uses % C::kSlots;
-        if (!bounded_wait(bar(C::kSlotFull + s), (slot_uses / C::kSlots) & 1u, abort_flag,
-                          p.status, kWaitLimit))
-          return false;
+        ++p_waits[t];
         fence_after_sync();
-        const uint32_t v_addr = sRing + s * C::kTileBytes;
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
           const uint64_t bdesc = sdesc_sw128(v_addr + kk * 16 * 128, C::kVLbo, 1024);
-          mma_ts(tmem + C::kColO, tmem + C::kColP + kk * 8, bdesc, C::kIdescO,
-                 (first && kk == 0) ? 0u : 1u);
+          mma_ts(tmem + C::kColO + t * D, tmem + C::kColS + t * kTile + kk * 8, bdesc,
+                 C::kIdescO, (first && kk == 0) ? 0u : 1u);
         }
-        mma_commit(bar(C::kPVDone));
-        mma_commit(bar(C::kSlotEmpty + s));
-        ++slot_uses;
         return true;
       };
       for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
         const ItemInfo it = item_info(p, order, prefix, i);
         if (it.nk == 0) continue;
+        const bool two = it.rows > kTile;
         if (!bounded_wait(bar(C::kQFull), q_uses & 1u, abort_flag, p.status, kWaitLimit)) {
           ok = false;
           break;
         }
         ++q_uses;
-        for (int j = 0; j < it.nk && ok; ++j) {
-          const uint32_t gg = g + j;
-          const uint32_t buf = gg & 1u, use = gg >> 1;
-          const uint32_t s = slot_uses % C::kSlots;
-          ok = bounded_wait(bar(C::kSlotFull + s), (slot_uses / C::kSlots) & 1u, abort_flag,
-                            p.status, kWaitLimit) &&
-               bounded_wait(bar(C::kSFree + buf), (use & 1u) ^ 1u, abort_flag, p.status,
-                            kWaitLimit);
-          if (!ok) break;
-          fence_after_sync();
-          const uint32_t k_addr = sRing + s * C::kTileBytes;
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
-            const uint64_t adesc = sdesc_sw128(sQ + off, 16, 1024);
-            const uint64_t bdesc = sdesc_sw128(k_addr + off, 16, 1024);
-            mma_ss(tmem + C::kColS + buf * kTile, adesc, bdesc, C::kIdescS, kk > 0 ? 1u : 0u);
-          }
-          mma_commit(bar(C::kSFull + buf));
-          mma_commit(bar(C::kSlotEmpty + s));
-          ++slot_uses;
-          if (j == it.nk - 1) mma_commit(bar(C::kQEmpty));
-          if (j >= 1) ok = issue_pv(gg - 1, j == 1);
+        // prologue: S0_0 (and S1_0) from K_0
+        uint32_t sk;
+        if (!wait_slot(sk)) {
+          ok = false;
+          break;
         }
-        if (ok) ok = issue_pv(g + it.nk - 1, it.nk == 1);
-        g += it.nk;
+        issue_s(0, sRing + sk * C::kTileBytes);
+        if (two) issue_s(1, sRing + sk * C::kTileBytes);
+        issued = 1;
+        mma_commit(bar(C::kSlotEmpty + sk));
+        ++slot_uses;
+        if (it.nk == 1) mma_commit(bar(C::kQEmpty));
+        for (int j = 0; j < it.nk && ok; ++j) {
+          uint32_t sv;
+          if (!wait_slot(sv)) {
+            ok = false;
+            break;
+          }
+          ++slot_uses;
+          const uint32_t v_addr = sRing + sv * C::kTileBytes;
+          const bool more = j + 1 < it.nk;
+          uint32_t sk2 = 0;
+          // tile 0: PV0_j, then S0_{j+1} (after the PV that reads P0 from S0)
+          if (!issue_pv(0, v_addr, j == 0)) {
+            ok = false;
+            break;
+          }
+          if (!more) mma_commit(bar(C::kOFull + 0));
+          if (more) {
+            if (!wait_slot(sk2)) {
+              ok = false;
+              break;
+            }
+            issue_s(0, sRing + sk2 * C::kTileBytes);
+          }
+          // tile 1: PV1_j, then S1_{j+1}
+          if (two) {
+            if (!issue_pv(1, v_addr, j == 0)) {
+              ok = false;
+              break;
+            }
+            if (!more) mma_commit(bar(C::kOFull + 1));
+          }
+          mma_commit(bar(C::kSlotEmpty + sv));
+          if (more) {
+            if (two) issue_s(1, sRing + sk2 * C::kTileBytes);
+            mma_commit(bar(C::kSlotEmpty + sk2));
+            ++slot_uses;
+            if (j + 2 == it.nk) mma_commit(bar(C::kQEmpty));
+          }
+        }
       }
       // every MMA issued so far has finished before TMEM is released
-      if (g > 0 || q_uses > 0) {
+      if (issued) {
         mma_commit(bar(C::kFinal));
         drain_wait(bar(C::kFinal), 0, kWaitLimit);
       }
@@ -275,18 +334,25 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncwarp();
   } else {
     // ================= softmax / correction / epilogue =================
+    // warps 2..5: tile 0, warps 6..9: tile 1; TMEM lane quadrant = warp % 4
+    const int t = (warp - 2) >> 2;
     const int quad = warp & 3;
     const int row = quad * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    const uint32_t colS = C::kColS + t * kTile;
+    const uint32_t colO = C::kColO + t * D;
     const float sl2 = p.scale_log2;
     const bool pos_scale = sl2 > 0.f;
     const float mul = pos_scale ? sl2 : 1.f;
-    uint32_t g = 0;
+    uint32_t s_waits = 0, o_waits = 0;
     bool ok = true;
     for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
       const ItemInfo it = item_info(p, order, prefix, i);
-      __nv_bfloat16 *dst = p.out + (static_cast<int64_t>(it.q_row0 + row) * p.H + it.head) * D;
-      const bool store = row < it.rows;
+      const int rows_t = it.rows - t * kTile;   // this tile's valid rows (may be <= 0)
+      if (rows_t <= 0) continue;                // tile absent: nothing issued for it
+      __nv_bfloat16 *dst =
+          p.out + (static_cast<int64_t>(it.q_row0 + t * kTile + row) * p.H + it.head) * D;
+      const bool store = row < rows_t;
       if (it.nk == 0) {
         if (store) {
           uint4 *d4 = reinterpret_cast<uint4 *>(dst);
@@ -297,23 +363,19 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < it.nk; ++j) {
-        const uint32_t gg = g + j;
-        const uint32_t buf = gg & 1u, use = gg >> 1;
-        ok = bounded_wait(bar(C::kSFull + buf), use & 1u, abort_flag, p.status, kWaitLimit);
+        ok = bounded_wait(bar(C::kSFull + t), s_waits & 1u, abort_flag, p.status, kWaitLimit);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
         }
+        ++s_waits;
         fence_after_sync();
         // all four 32-column loads in flight, then one wait
         uint32_t sr[kTile];
 #pragma unroll
         for (int c = 0; c < kTile / 32; ++c)
-          tmem_ld32(lane_base + C::kColS + buf * kTile + c * 32,
-                    *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+          tmem_ld32(lane_base + colS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
         tmem_wait_ld();
-        fence_before_sync();
-        mbar_arrive(bar(C::kSFree + buf));
         // x = raw scores as pairs; with a positive scale the scale is folded
         // into the exponent's FFMA, otherwise the scores are scaled first
         float2 x[kTile / 2];
@@ -325,15 +387,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
           for (int c = 0; c < kTile / 2; ++c) x[c] = __fmul2_rn(x[c], s2);
         }
-        if (j == it.nk - 1) {
-          const int valid = it.lk - j * kTile;
+        if (key_tile(it, j) == it.nk - 1) {
+          const int valid = it.lk - (it.nk - 1) * kTile;
 #pragma unroll
           for (int c = 0; c < kTile / 2; ++c) {
             if (2 * c >= valid) x[c].x = -INFINITY;
             if (2 * c + 1 >= valid) x[c].y = -INFINITY;
           }
         }
-        // row maximum: eight independent chains of 3-input max, fixed combine
+        // row maximum: eight chains of 3-input max, fixed combine
         float mx8[8];
 #pragma unroll
         for (int e = 0; e < 8; ++e) mx8[e] = fmaxf(x[e].x, x[e].y);
@@ -357,63 +419,56 @@ __global__ void __launch_bounds__(kThreads, 1)
         uint32_t pk[kTile / 2];
 #pragma unroll
         for (int c = 0; c < kTile / 2; ++c) {
-          const float2 t = __ffma2_rn(x[c], mul2, negm2);
-          const float2 pp = make_float2(ex2(t.x), ex2(t.y));
+          const float2 tt = __ffma2_rn(x[c], mul2, negm2);
+          const float2 pp = make_float2(ex2(tt.x), ex2(tt.y));
           sum8[c & 7] = __fadd2_rn(sum8[c & 7], pp);
           pk[c] = pack_bf16x2(pp.x, pp.y);
         }
         const float2 s01 = __fadd2_rn(__fadd2_rn(sum8[0], sum8[1]), __fadd2_rn(sum8[2], sum8[3]));
         const float2 s45 = __fadd2_rn(__fadd2_rn(sum8[4], sum8[5]), __fadd2_rn(sum8[6], sum8[7]));
         const float2 s8 = __fadd2_rn(s01, s45);
-        const float sum = s8.x + s8.y;
-        l = l * alpha + sum;
-        if (j >= 1) {
-          // PV of the previous tile must be done: it updates O and reads P
-          ok = bounded_wait(bar(C::kPVDone), (gg - 1) & 1u, abort_flag, p.status, kWaitLimit);
-          if (!__all_sync(0xffffffffu, ok)) {
-            ok = false;
-            break;
-          }
-          fence_after_sync();
-          if (__any_sync(0xffffffffu, rescale)) {
+        l = l * alpha + (s8.x + s8.y);
+        // S_j complete implies the PV issued before it is complete: O is
+        // current and can be rescaled in place
+        if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t r[32];
-              tmem_ld32(lane_base + C::kColO + c * 32, r);
-              tmem_wait_ld();
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t r[32];
+            tmem_ld32(lane_base + colO + c * 32, r);
+            tmem_wait_ld();
 #pragma unroll
-              for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-              tmem_st32(lane_base + C::kColO + c * 32, r);
-            }
+            for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
+            tmem_st32(lane_base + colO + c * 32, r);
           }
         }
+        // P over the first 64 columns of this tile's S buffer
         {
           uint32_t r[32];
 #pragma unroll
           for (int e = 0; e < 32; ++e) r[e] = pk[e];
-          tmem_st32(lane_base + C::kColP, r);
+          tmem_st32(lane_base + colS, r);
 #pragma unroll
           for (int e = 0; e < 32; ++e) r[e] = pk[32 + e];
-          tmem_st32(lane_base + C::kColP + 32, r);
+          tmem_st32(lane_base + colS + 32, r);
         }
         tmem_wait_st();
         fence_before_sync();
-        mbar_arrive(bar(C::kPReady));
+        mbar_arrive(bar(C::kPReady + t));
       }
       if (!ok) break;
-      // epilogue: wait for the last PV, normalise, store the valid rows
-      ok = bounded_wait(bar(C::kPVDone), (g + it.nk - 1) & 1u, abort_flag, p.status,
-                        kWaitLimit);
+      // epilogue: wait for this tile's last PV, normalise, store valid rows
+      ok = bounded_wait(bar(C::kOFull + t), o_waits & 1u, abort_flag, p.status, kWaitLimit);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
       }
+      ++o_waits;
       fence_after_sync();
       const float inv = 1.f / l;
 #pragma unroll
       for (int c = 0; c < D / 32; ++c) {
         uint32_t r[32];
-        tmem_ld32(lane_base + C::kColO + c * 32, r);
+        tmem_ld32(lane_base + colO + c * 32, r);
         tmem_wait_ld();
         if (store) {
           uint4 *d4 = reinterpret_cast<uint4 *>(dst + c * 32);
@@ -428,7 +483,6 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
         }
       }
-      g += it.nk;
     }
   }
 

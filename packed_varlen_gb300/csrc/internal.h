@@ -5,7 +5,7 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
-#include "../../include/packedattn.h"
+#include "packedattn.h"
 
 namespace pa {
 

@@ -14,7 +14,7 @@
 
 #include <stdint.h>
 
-#include "../../include/packedattn.h"
+#include "packedattn.h"
 
 namespace pa {
 

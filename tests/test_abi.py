@@ -108,4 +108,5 @@ def test_num_work_items_matches_oracle(lib):
     for L in ([37, 64], [0, 129, 128, 1], [33024], [16640, 4352, 7000, 2500]):
         cu = oracle.cu_seqlens_from_lengths(L).tolist()
         for H in (1, 24):
-            assert pv.varlen_num_work_items(cu, H) == len(oracle.work_order(L, L, H, 128))
+            for tile in (128, pv.VARLEN_TILE_M):
+                assert pv.varlen_num_work_items(cu, H, tile) == len(oracle.work_order(L, L, H, tile))

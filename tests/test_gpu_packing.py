@@ -79,7 +79,7 @@ def test_work_order(pv, lq, lk, H):
     lk = lq if lk is None else lk
     cu_q = torch.tensor(oracle.cu_seqlens_from_lengths(lq), device="cuda")
     cu_k = torch.tensor(oracle.cu_seqlens_from_lengths(lk), device="cuda")
-    want = oracle.work_order(lq, lk, H, 128)
+    want = oracle.work_order(lq, lk, H, pv.VARLEN_TILE_M)
     got = pv.varlen_work_order(cu_q, cu_k, H, len(want))
     assert [tuple(r) for r in got.cpu().tolist()] == want
     assert pv.get_device_status() == 0
@@ -91,13 +91,13 @@ def test_work_order_large_batch(pv):
     lk = rng.integers(0, 50, size=1024).tolist()   # many ties
     cu_q = torch.tensor(oracle.cu_seqlens_from_lengths(lq), device="cuda")
     cu_k = torch.tensor(oracle.cu_seqlens_from_lengths(lk), device="cuda")
-    want = oracle.work_order(lq, lk, 2, 128)
+    want = oracle.work_order(lq, lk, 2, pv.VARLEN_TILE_M)
     got = pv.varlen_work_order(cu_q, cu_k, 2, len(want))
     assert [tuple(r) for r in got.cpu().tolist()] == want
 
 
 def test_work_order_capacity(pv):
     cu = torch.tensor([0, 300], dtype=torch.int32, device="cuda")
-    got = pv.varlen_work_order(cu, cu, 2, 4)
+    got = pv.varlen_work_order(cu, cu, 2, 4, tile_m=128)
     assert got.cpu().tolist() == [[0, 0, 0], [0, 0, 1], [0, 0, 2], [0, 1, 0]]
     assert pv.get_device_status() == 5
