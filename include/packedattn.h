@@ -52,6 +52,7 @@ typedef enum {
 #define PA_DEVICE_ERR_LENGTH 4       /* a negative length, or a sum above INT32_MAX, in
                                         pa_cu_seqlens_from_lengths */
 #define PA_DEVICE_ERR_CAPACITY 5     /* pa_varlen_work_order: more items than capacity */
+#define PA_DEVICE_ERR_SMEM_ALIGN 6   /* dynamic shared memory not 1024-byte aligned (kernel skipped) */
 
 /* Largest batch (number of packed sequences) the attention kernels accept. */
 #define PA_MAX_BATCH 1024

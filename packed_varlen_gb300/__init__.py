@@ -24,7 +24,7 @@ STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED",
                 3: "PA_ERR_MISALIGNED", 4: "PA_ERR_CUDA", 5: "PA_ERR_DEVICE"}
 DEVICE_ERRORS = {0: "PA_DEVICE_OK", 1: "PA_DEVICE_ERR_CU_SEQLENS", 2: "PA_DEVICE_ERR_MAX_LEN",
                  3: "PA_DEVICE_ERR_TIMEOUT", 4: "PA_DEVICE_ERR_LENGTH",
-                 5: "PA_DEVICE_ERR_CAPACITY"}
+                 5: "PA_DEVICE_ERR_CAPACITY", 6: "PA_DEVICE_ERR_SMEM_ALIGN"}
 MAX_BATCH = 1024
 VARLEN_TILE_M = 256
 

@@ -52,11 +52,15 @@ constexpr long long kWaitLimit = 4000000000LL;  // clock cycles (~2 s)
 constexpr long long kDrainLimit = 400000000LL;  // teardown after an abort (~0.2 s)
 constexpr float kRescaleThreshold = 8.0f;       // log2 units
 
-template <int D>
+// Shared-memory plan for head dim D, kSlots K/V ring slots and a work list
+// of up to kMaxSeqs sequences.  The dynamic shared-memory window starts
+// 1024-byte aligned (checked at run time), so no alignment slack is added.
+template <int D, int kSlots_, int kMaxSeqs_>
 struct Cfg {
+  static constexpr int kSlots = kSlots_;
+  static constexpr int kMaxSeqs = kMaxSeqs_;
   static constexpr int kHalfBytes = kTile * 64 * 2;         // 128 rows x 128 B
   static constexpr int kTileBytes = kTile * D * 2;          // one Q/K/V tile
-  static constexpr int kSlots = D == 128 ? 4 : 8;
   static constexpr int kQOff = 0;                           // Q0, Q1
   static constexpr int kRingOff = 2 * kTileBytes;
   static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
@@ -66,7 +70,8 @@ struct Cfg {
   static constexpr int kNumBars = 9 + 2 * kSlots;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;   // tmem base, abort flag
   static constexpr int kSchedOff = (kMiscOff + 16 + 127) / 128 * 128;
-  static constexpr int kSmemBytes = kSchedOff + (2 * PA_MAX_BATCH + 1) * 4 + 1024;
+  static constexpr int kSmemBytes = kSchedOff + (2 * kMaxSeqs + 1) * 4;
+  static_assert(kSmemBytes <= 232448, "shared memory plan exceeds the per-CTA limit");
   // TMEM columns: S_t at 128 t (P_t over its first 64), O_t at 256 + D t
   static constexpr uint32_t kColS = 0;
   static constexpr uint32_t kColO = 256;
@@ -123,24 +128,27 @@ __device__ __forceinline__ ItemInfo item_info(const TcParams &p, const int32_t *
   return it;
 }
 
-template <int D>
+template <int D, int kSlots, int kMaxSeqs>
 __global__ void __launch_bounds__(kThreads, 1)
     varlen_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_k,
                           const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
-  using C = Cfg<D>;
+  using C = Cfg<D, kSlots, kMaxSeqs>;
   extern __shared__ uint8_t smem_raw[];
-  // 1024-byte aligned base (128-byte swizzle atoms)
-  const uint32_t raw = smem_u32(smem_raw);
-  const uint32_t base = (raw + 1023u) & ~1023u;
-  uint8_t *gbase = smem_raw + (base - raw);
+  // 128-byte swizzle atoms need a 1024-byte aligned base
+  const uint32_t base = smem_u32(smem_raw);
+  if (base & 1023u) {
+    if (threadIdx.x == 0) record_error(p.status, PA_DEVICE_ERR_SMEM_ALIGN);
+    return;
+  }
+  uint8_t *gbase = smem_raw;
   const uint32_t sQ = base + C::kQOff;
   const uint32_t sRing = base + C::kRingOff;
   auto bar = [&](int idx) -> uint32_t { return base + C::kBarOff + 8u * idx; };
   uint32_t *tmem_base_ptr = reinterpret_cast<uint32_t *>(gbase + C::kMiscOff);
   volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(gbase + C::kMiscOff + 4);
   int32_t *order = reinterpret_cast<int32_t *>(gbase + C::kSchedOff);
-  int32_t *prefix = order + PA_MAX_BATCH;
+  int32_t *prefix = order + kMaxSeqs;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 
@@ -164,7 +172,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_alloc(base + C::kMiscOff, C::kTmemCols);
   // the ring is free until the first load: use it for the build's temporaries
   int32_t *tmp = reinterpret_cast<int32_t *>(gbase + C::kRingOff);
-  sched_build(order, prefix, tmp, tmp + PA_MAX_BATCH, p.cu_q, p.cu_k, p.batch, p.H,
+  sched_build(order, prefix, tmp, tmp + kMaxSeqs, p.cu_q, p.cu_k, p.batch, p.H,
               kItemRows, p.total_q, p.total_k, p.max_q, p.max_k, p.status, blockIdx.x == 0);
   fence_before_sync();
   __syncthreads();
@@ -239,28 +247,34 @@ __global__ void __launch_bounds__(kThreads, 1)
                             p.status, kWaitLimit);
       };
       // S_t = Q_t K^T into S buffer t (Q/K K-major, SBO = 8 rows x 128 B)
-      auto issue_s = [&](int t, uint32_t k_addr) {
+      // (descriptors advance by adding the byte offset >> 4 to the start
+      // address field; every operand lies below 256 KB, so nothing carries)
+      const uint64_t qdesc0 = sdesc_sw128(sQ, 16, 1024);
+      const uint64_t kdesc0 = sdesc_sw128(sRing, 16, 1024);
+      const uint64_t vdesc0 = sdesc_sw128(sRing, C::kVLbo, 1024);
+      const uint32_t d_s = tmem + C::kColS, d_o = tmem + C::kColO;
+      auto issue_s = [&](int t, uint32_t slot) {
+        const uint64_t a0 = qdesc0 + ((t * C::kTileBytes) >> 4);
+        const uint64_t b0 = kdesc0 + ((slot * C::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * C::kHalfBytes + (kk & 3) * 32;
-          const uint64_t adesc = sdesc_sw128(sQ + t * C::kTileBytes + off, 16, 1024);
-          const uint64_t bdesc = sdesc_sw128(k_addr + off, 16, 1024);
-          mma_ss(tmem + C::kColS + t * kTile, adesc, bdesc, C::kIdescS, kk > 0 ? 1u : 0u);
+          const uint32_t off = ((kk >> 2) * C::kHalfBytes + (kk & 3) * 32) >> 4;
+          mma_ss(d_s + t * kTile, a0 + off, b0 + off, C::kIdescS, kk > 0 ? 1u : 0u);
         }
         mma_commit(bar(C::kSFull + t));
       };
       // O_t += P_t V once tile t's softmax has written P_t
-      auto issue_pv = [&](int t, uint32_t v_addr, bool first) -> bool {
+      auto issue_pv = [&](int t, uint32_t slot, bool first) -> bool {
         if (!bounded_wait(bar(C::kPReady + t), p_waits[t] & 1u, abort_flag, p.status,
                           kWaitLimit))
           return false;
         ++p_waits[t];
         fence_after_sync();
+        const uint64_t b0 = vdesc0 + ((slot * C::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
-          const uint64_t bdesc = sdesc_sw128(v_addr + kk * 16 * 128, C::kVLbo, 1024);
-          mma_ts(tmem + C::kColO + t * D, tmem + C::kColS + t * kTile + kk * 8, bdesc,
-                 C::kIdescO, (first && kk == 0) ? 0u : 1u);
+          mma_ts(d_o + t * D, d_s + t * kTile + kk * 8, b0 + ((kk * 16 * 128) >> 4), C::kIdescO,
+                 (first && kk == 0) ? 0u : 1u);
         }
         return true;
       };
@@ -279,8 +293,8 @@ __global__ void __launch_bounds__(kThreads, 1)
           ok = false;
           break;
         }
-        issue_s(0, sRing + sk * C::kTileBytes);
-        if (two) issue_s(1, sRing + sk * C::kTileBytes);
+        issue_s(0, sk);
+        if (two) issue_s(1, sk);
         issued = 1;
         mma_commit(bar(C::kSlotEmpty + sk));
         ++slot_uses;
@@ -292,11 +306,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           ++slot_uses;
-          const uint32_t v_addr = sRing + sv * C::kTileBytes;
           const bool more = j + 1 < it.nk;
           uint32_t sk2 = 0;
           // tile 0: PV0_j, then S0_{j+1} (after the PV that reads P0 from S0)
-          if (!issue_pv(0, v_addr, j == 0)) {
+          if (!issue_pv(0, sv, j == 0)) {
             ok = false;
             break;
           }
@@ -306,11 +319,11 @@ __global__ void __launch_bounds__(kThreads, 1)
               ok = false;
               break;
             }
-            issue_s(0, sRing + sk2 * C::kTileBytes);
+            issue_s(0, sk2);
           }
           // tile 1: PV1_j, then S1_{j+1}
           if (two) {
-            if (!issue_pv(1, v_addr, j == 0)) {
+            if (!issue_pv(1, sv, j == 0)) {
               ok = false;
               break;
             }
@@ -318,7 +331,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           }
           mma_commit(bar(C::kSlotEmpty + sv));
           if (more) {
-            if (two) issue_s(1, sRing + sk2 * C::kTileBytes);
+            if (two) issue_s(1, sk2);
             mma_commit(bar(C::kSlotEmpty + sk2));
             ++slot_uses;
             if (j + 2 == it.nk) mma_commit(bar(C::kQEmpty));
@@ -528,7 +541,7 @@ bool make_map(CUtensorMap *map, const void *ptr, int rows, int H, int D) {
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int D>
+template <int D, int kSlots, int kMaxSeqs>
 cudaError_t launch_tc(const VarlenArgs &a, cudaStream_t stream) {
   CUtensorMap mq, mk, mv;
   if (!make_map(&mq, a.q, a.total_q, a.H, D) || !make_map(&mk, a.k, a.total_k, a.H, D) ||
@@ -546,18 +559,22 @@ cudaError_t launch_tc(const VarlenArgs &a, cudaStream_t stream) {
   p.max_k = a.max_k;
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.status = a.status;
-  const int smem = Cfg<D>::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(varlen_attn_tc_kernel<D>,
+  const int smem = Cfg<D, kSlots, kMaxSeqs>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(varlen_attn_tc_kernel<D, kSlots, kMaxSeqs>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
   if (e != cudaSuccess) return e;
-  varlen_attn_tc_kernel<D><<<a.num_sms, kThreads, smem, stream>>>(mq, mk, mv, p);
+  varlen_attn_tc_kernel<D, kSlots, kMaxSeqs><<<a.num_sms, kThreads, smem, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
+// Ring depth: with D = 128 a fifth 32 KB slot fits only beside a work list
+// of at most 256 sequences; larger batches use four slots.
 cudaError_t launch_varlen_attn(const VarlenArgs &a, cudaStream_t stream) {
-  return a.D == 64 ? launch_tc<64>(a, stream) : launch_tc<128>(a, stream);
+  if (a.D == 64) return launch_tc<64, 10, PA_MAX_BATCH>(a, stream);
+  if (a.batch <= 256) return launch_tc<128, 5, 256>(a, stream);
+  return launch_tc<128, 4, PA_MAX_BATCH>(a, stream);
 }
 
 }  // namespace pa
