@@ -121,6 +121,22 @@ def max_over_ranks(value: float, dist=None, device=None) -> float:
     return float(t.item())
 
 
+class L2Flusher:
+    """Empties L2 between timed iterations, outside the timed events: writes a
+    buffer larger than L2 (evicting everything), then reads a second one so
+    that the dirty lines of the write are written back before timing starts
+    and L2 holds only clean lines."""
+
+    def __init__(self, device, nbytes: int = L2_FLUSH_BYTES):
+        self.w = torch.empty(nbytes // 4, dtype=torch.float32, device=device)
+        self.r = torch.ones(nbytes // 4, dtype=torch.float32, device=device)
+        self.sink = torch.empty((), dtype=torch.float32, device=device)
+
+    def flush(self):
+        self.w.zero_()
+        torch.sum(self.r, dim=0, out=self.sink)
+
+
 class ClockSampler:
     """nvidia-smi clock/throttle samples taken while the timed region runs."""
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -265,7 +281,7 @@ def run_ours(args):
     qf = torch.empty(T, H, D, dtype=torch.bfloat16, device=dev)
     kf, vf, of = torch.empty_like(qf), torch.empty_like(qf), torch.empty_like(qf)
     out_pad = torch.zeros_like(q_pad)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flusher = L2Flusher(dev)
     scale = 1.0 / math.sqrt(D)
 
     attn_ev = []
@@ -301,7 +317,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     step_ev = []
     for _ in range(args.steps):
-        flush.zero_()
+        flusher.flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         step(record=True)
@@ -336,7 +352,7 @@ def run_ours(args):
     torch.cuda.synchronize()
     e2e_ms = []
     for _ in range(max(3, min(args.steps, 10))):
-        flush.zero_()
+        flusher.flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         e2e_step()
@@ -358,7 +374,7 @@ def run_ours(args):
     for lb, la in sorted(set(bw.layers)):
         ts = []
         for _ in range(20):
-            flush.zero_()
+            flusher.flush()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
             pv.block_window_attn_fwd(bq, bk, bv, bw.block, lb, la, out=bo)
@@ -394,7 +410,8 @@ def run_ours(args):
             "config": {"workload": WORKLOAD, "batch": B, "lengths": L, "tokens": T, "H": H,
                        "D": D, "s_max": S, "useful_flops_per_step": flops,
                        "step": "cu_seqlens + pack q,k,v + varlen attention + unpack",
-                       "l2": "flushed between timed steps (512 MB write outside the events); "
+                       "l2": "flushed between timed steps outside the events (512 MB write, then "
+                             "512 MB read so L2 holds clean lines); "
                              "padded inputs 3 x %.0f MB also exceed L2"
                              % (q_pad.numel() * 2 / 2**20),
                        "parallelism": f"{ws} independent batches (one per GPU)"},
@@ -435,6 +452,8 @@ def run_attn_only(args):
     dev = torch.device("cuda", 0)
     pv.load_library()
     pv.get_device_status()
+    if args.workload == "token2wav":
+        return run_block_window_only(args, dev)
     if args.workload in workloads.VARLEN_CONFIGS:
         w = workloads.VARLEN_CONFIGS[args.workload]()
     else:
@@ -443,7 +462,7 @@ def run_attn_only(args):
     q, k, v = w.q.to(dev), w.k.to(dev), w.v.to(dev)
     cu = pv.cu_seqlens_from_lengths(torch.tensor(w.lengths_q, dtype=torch.int32, device=dev))
     out = torch.empty_like(q)
-    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=dev)
+    flusher = L2Flusher(dev)
     flops = 4 * w.H * w.D * sum(a * b for a, b in zip(w.lengths_q, w.lengths_k))
     stream = torch.cuda.current_stream()
     for _ in range(args.warmup):
@@ -451,7 +470,7 @@ def run_attn_only(args):
     torch.cuda.synchronize()
     ts = []
     for _ in range(args.steps):
-        flush.zero_()
+        flusher.flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         pv.varlen_attn_fwd(q, k, v, cu, cu, max(w.lengths_q), max(w.lengths_k), out=out)
@@ -463,6 +482,38 @@ def run_attn_only(args):
     ms = statistics.median(a.elapsed_time(b) for a, b in ts)
     print(json.dumps({"workload": w.name, "lengths": w.lengths_q, "H": w.H, "D": w.D,
                       "attn_ms": ms, "tflops": flops / (ms * 1e-3) / 1e12}), flush=True)
+    return 0
+
+
+def run_block_window_only(args, dev):
+    """Block-window layers alone (profiling): median us per layer type with a
+    clean L2 before each launch, and a one-CTA kernel for the launch floor."""
+    import packed_varlen_gb300 as pv
+    bw = workloads.token2wav()
+    bq, bk, bv = bw.q.to(dev), bw.k.to(dev), bw.v.to(dev)
+    bo = torch.empty_like(bq)
+    flusher = L2Flusher(dev)
+    stream = torch.cuda.current_stream()
+    lens = torch.tensor([5, 7], dtype=torch.int32, device=dev)
+    cu = torch.empty(3, dtype=torch.int32, device=dev)
+    res = {}
+    cases = [("0,0", lambda: pv.block_window_attn_fwd(bq, bk, bv, 24, 0, 0, out=bo)),
+             ("1,1", lambda: pv.block_window_attn_fwd(bq, bk, bv, 24, 1, 1, out=bo)),
+             ("floor", lambda: pv.cu_seqlens_from_lengths(lens, out=cu))]
+    for name, fn in cases:
+        for _ in range(args.warmup):
+            fn()
+        ts = []
+        for _ in range(args.steps):
+            flusher.flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            ts.append((e0, e1))
+        torch.cuda.synchronize()
+        res[name] = 1e3 * statistics.median(a.elapsed_time(b) for a, b in ts)
+    print(json.dumps({"workload": "token2wav", "us": res}), flush=True)
     return 0
 
 

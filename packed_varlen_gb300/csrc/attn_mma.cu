@@ -1,14 +1,21 @@
-// Block-window attention (Token2Wav DiT): register-tiled flash attention on
-// warp-level mma.sync (bf16 in, fp32 accumulate), cp.async double-buffered
-// K/V tiles in swizzled shared memory, online softmax in fp32 with quad
-// shuffles.  The windows are short (24-72 keys per query) and the layer is
-// bound by HBM traffic and launch latency, not by the tensor pipe.
+// Block-window attention of the Token2Wav DiT ("[Perf][Model] Use
+// block-sparse attention in Qwen2.5-Omni Token2Wav DiT", Change): frames are
+// grouped in blocks; query i sees key j iff j < n and
+//   -look_back <= block(j) - block(i) <= look_ahead.
 //
-// Block window: "[Perf][Model] Use block-sparse attention in Qwen2.5-Omni
-// Token2Wav DiT" (Change).  A CTA owns 64 query rows; it visits only the key
-// rows [(first_block - look_back) * block, (last_block + 1 + look_ahead) *
-// block) clipped to [0, n) and masks by the integer block difference, so no
-// mask tensor exists and nothing is decided on the host from device data.
+// The layer is small (n = 2400, H = 16, D = 64: 19.7 MB of q/k/v/out) and its
+// windows are 24-72 keys wide, so it is bound by memory latency, HBM traffic
+// and launch cost, not by the tensor pipe.  The kernel therefore optimises
+// for memory-level parallelism: a CTA owns 64 query rows of one head and
+// issues the copies of its query tile and of up to kStages 32-key K/V tiles
+// of its window at once (cp.async), then runs a register-tiled flash
+// attention on warp-level mma.sync (bf16 in, fp32 accumulate) with online
+// softmax.  Each query row carries its own key interval [lo, hi) computed
+// from the integer block parameters, so masking is two compares per score,
+// no mask tensor exists, and nothing is read back from the device to decide
+// whether masking applies.  A warp (16 rows, at most two 24-frame blocks)
+// skips every key tile outside its rows' windows, so the scores computed
+// stay close to the allowed ones.
 #include <cuda_bf16.h>
 #include <math.h>
 
@@ -18,22 +25,17 @@
 namespace pa {
 namespace {
 
-constexpr int kBr = 64;  // query rows per CTA: 4 warps x 16
-constexpr int kBc = 64;  // keys per tile
+constexpr int kBr = 64;      // query rows per CTA: 4 warps x 16
+constexpr int kBc = 32;      // keys per tile
 constexpr int kThreads = 128;
+constexpr int kStages = 4;   // K/V tiles in flight (a Token2Wav CTA window is <= 144 keys)
 
-struct MmaParams {
+struct BwParams {
   const __nv_bfloat16 *q, *k, *v;
   __nv_bfloat16 *out;
   int64_t row_stride;  // elements between consecutive tokens (H * D)
   float scale_log2;    // scale * log2(e)
-  int H;
-  // varlen
-  const int32_t *cu_q, *cu_k;
-  int total_q, total_k, max_q, max_k;
-  // block window
   int n, block, look_back, look_ahead;
-  int32_t *status;
 };
 
 __device__ __forceinline__ uint32_t smem_addr(const void *p) {
@@ -107,56 +109,60 @@ __device__ __forceinline__ void load_tile(uint32_t dst, const __nv_bfloat16 *bas
   }
 }
 
-template <int D, bool kBlockWindow>
-__global__ void __launch_bounds__(kThreads) attn_mma_kernel(const MmaParams p) {
+// Key interval of query i: [(b - look_back) * block, (b + 1 + look_ahead) * block)
+// clipped to [0, n), b = block of i.
+__device__ __forceinline__ void window(const BwParams &p, int i, int &lo, int &hi) {
+  const int64_t b = i / p.block;
+  const int64_t l = (b - p.look_back) * p.block;
+  const int64_t h = (b + 1 + p.look_ahead) * p.block;
+  lo = static_cast<int>(l > 0 ? l : 0);
+  hi = static_cast<int>(h < p.n ? h : p.n);
+}
+
+template <int D>
+__global__ void __launch_bounds__(kThreads, D == 64 ? 4 : 2) block_window_kernel(const BwParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   const uint32_t sQ = smem_addr(smem);
   const uint32_t sK = sQ + kBr * D * 2;
-  const uint32_t sV = sK + 2 * kBc * D * 2;
+  const uint32_t sV = sK + kStages * kBc * D * 2;
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, t4 = lane & 3;
   const int h = blockIdx.y;
   const int seq = blockIdx.z;
 
-  int64_t q_row0, k_base;  // global rows of the tile's first query / sequence's key 0
-  int q_rel0, n_rows, k_lo, k_hi;
-  if (kBlockWindow) {
-    q_rel0 = blockIdx.x * kBr;
-    if (q_rel0 >= p.n) return;
-    n_rows = min(kBr, p.n - q_rel0);
-    q_row0 = static_cast<int64_t>(seq) * p.n + q_rel0;
-    k_base = static_cast<int64_t>(seq) * p.n;
-    const int64_t first_blk = q_rel0 / p.block;
-    const int64_t last_blk = (q_rel0 + n_rows - 1) / p.block;
-    const int64_t lo = (first_blk - p.look_back) * p.block;
-    const int64_t hi = (last_blk + 1 + p.look_ahead) * p.block;
-    k_lo = static_cast<int>(lo > 0 ? lo : 0);
-    k_hi = static_cast<int>(hi < p.n ? hi : p.n);
-  } else {
-    int err;
-    const SeqBounds sb = seq_bounds(p.cu_q, p.cu_k, seq, p.total_q, p.total_k, p.max_q,
-                                    p.max_k, err);
-    if (err) {
-      if (blockIdx.x == 0 && h == 0 && tid == 0) record_error(p.status, err);
-      return;
-    }
-    q_rel0 = blockIdx.x * kBr;
-    if (q_rel0 >= sb.lq) return;
-    n_rows = min(kBr, sb.lq - q_rel0);
-    q_row0 = static_cast<int64_t>(sb.q0) + q_rel0;
-    k_base = sb.k0;
-    k_lo = 0;
-    k_hi = sb.lk;
-  }
+  const int q_rel0 = blockIdx.x * kBr;
+  if (q_rel0 >= p.n) return;
+  const int n_rows = min(kBr, p.n - q_rel0);
+  const int64_t q_row0 = static_cast<int64_t>(seq) * p.n + q_rel0;
+  const int64_t k_base = static_cast<int64_t>(seq) * p.n;
+  int k_lo, k_hi, unused;
+  window(p, q_rel0, k_lo, unused);
+  window(p, q_rel0 + n_rows - 1, unused, k_hi);
   const int64_t stride = p.row_stride;
+  const int ntiles = (k_hi - k_lo + kBc - 1) / kBc;
 
+  // every copy of the first kStages tiles is issued before any wait:
+  // group 0 = Q + tile 0, group s = tile s (empty groups past the window)
   load_tile<D, kBr>(sQ, p.q, q_row0, n_rows, stride, h);
-  if (k_lo < k_hi) {
-    load_tile<D, kBc>(sK, p.k, k_base + k_lo, k_hi - k_lo, stride, h);
-    load_tile<D, kBc>(sV, p.v, k_base + k_lo, k_hi - k_lo, stride, h);
+  for (int s = 0; s < kStages; ++s) {
+    if (s < ntiles) {
+      const int kt = k_lo + s * kBc;
+      load_tile<D, kBc>(sK + s * kBc * D * 2, p.k, k_base + kt, k_hi - kt, stride, h);
+      load_tile<D, kBc>(sV + s * kBc * D * 2, p.v, k_base + kt, k_hi - kt, stride, h);
+    }
+    cp_async_commit();
   }
-  cp_async_commit();
+
+  // the thread's two query rows and their key intervals
+  const int row_in_tile[2] = {warp * 16 + g, warp * 16 + g + 8};
+  int lo[2], hi[2];
+#pragma unroll
+  for (int r = 0; r < 2; ++r) window(p, q_rel0 + row_in_tile[r], lo[r], hi[r]);
+  // keys any of the warp's 16 rows may see (intervals grow with the row)
+  int w_lo, w_hi;
+  window(p, q_rel0 + warp * 16, w_lo, unused);
+  window(p, q_rel0 + warp * 16 + 15, unused, w_hi);
 
   float o[D / 8][4];
 #pragma unroll
@@ -165,25 +171,10 @@ __global__ void __launch_bounds__(kThreads) attn_mma_kernel(const MmaParams p) {
   float l_run[2] = {0.f, 0.f};
   uint32_t qf[D / 16][4];
 
-  const int row_in_tile[2] = {warp * 16 + g, warp * 16 + g + 8};
-  const int ntiles = (k_hi - k_lo + kBc - 1) / kBc;
-
-  if (ntiles == 0) {
-    cp_async_wait<0>();
-    __syncthreads();
-  }
   for (int it = 0; it < ntiles; ++it) {
-    const int kt = k_lo + it * kBc;
-    const int buf = it & 1;
-    if (it + 1 < ntiles) {
-      const int kn = kt + kBc;
-      load_tile<D, kBc>(sK + (buf ^ 1) * kBc * D * 2, p.k, k_base + kn, k_hi - kn, stride, h);
-      load_tile<D, kBc>(sV + (buf ^ 1) * kBc * D * 2, p.v, k_base + kn, k_hi - kn, stride, h);
-      cp_async_commit();
-      cp_async_wait<1>();
-    } else {
-      cp_async_wait<0>();
-    }
+    const int stage = it % kStages;
+    // groups 0..it are complete once at most kStages - 1 newer ones are pending
+    cp_async_wait<kStages - 1>();
     __syncthreads();
     if (it == 0) {
 #pragma unroll
@@ -193,10 +184,13 @@ __global__ void __launch_bounds__(kThreads) attn_mma_kernel(const MmaParams p) {
         ldsm_x4(sQ + tile_off<D>(r, c), qf[kk][0], qf[kk][1], qf[kk][2], qf[kk][3]);
       }
     }
-    const uint32_t tK = sK + buf * kBc * D * 2;
-    const uint32_t tV = sV + buf * kBc * D * 2;
+    const int kt = k_lo + it * kBc;
+    const uint32_t tK = sK + stage * kBc * D * 2;
+    const uint32_t tV = sV + stage * kBc * D * 2;
+    const bool active = kt < w_hi && kt + kBc > w_lo;  // warp-uniform
 
     float s[kBc / 8][4];
+    if (active) {
 #pragma unroll
     for (int i = 0; i < kBc / 8; ++i) s[i][0] = s[i][1] = s[i][2] = s[i][3] = 0.f;
 #pragma unroll
@@ -211,19 +205,14 @@ __global__ void __launch_bounds__(kThreads) attn_mma_kernel(const MmaParams p) {
         mma_bf16(s[2 * pp + 1], qf[kk], b2, b3);
       }
     }
-    // scale into log2 units and mask
+    // scale into log2 units; keys outside the row's window -> -inf
 #pragma unroll
     for (int nb = 0; nb < kBc / 8; ++nb) {
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
         const int key = kt + nb * 8 + 2 * t4 + (e & 1);
-        bool ok = key < k_hi;
-        if (kBlockWindow) {
-          const int qrel = q_rel0 + row_in_tile[e >> 1];
-          const int diff = key / p.block - qrel / p.block;
-          ok = ok && diff >= -p.look_back && diff <= p.look_ahead;
-        }
-        s[nb][e] = ok ? s[nb][e] * p.scale_log2 : -INFINITY;
+        const int r = e >> 1;
+        s[nb][e] = (key >= lo[r] && key < hi[r]) ? s[nb][e] * p.scale_log2 : -INFINITY;
       }
     }
     // online softmax for the thread's two rows
@@ -270,8 +259,17 @@ __global__ void __launch_bounds__(kThreads) attn_mma_kernel(const MmaParams p) {
         mma_bf16(o[2 * pp + 1], a, b2, b3);
       }
     }
-    __syncthreads();
+    }  // active
+    __syncthreads();  // stage `stage` is free again
+    const int nxt = it + kStages;
+    if (nxt < ntiles) {
+      const int kn = k_lo + nxt * kBc;
+      load_tile<D, kBc>(tK, p.k, k_base + kn, k_hi - kn, stride, h);
+      load_tile<D, kBc>(tV, p.v, k_base + kn, k_hi - kn, stride, h);
+    }
+    cp_async_commit();  // (possibly empty) group keeps the group count aligned
   }
+  cp_async_wait<0>();  // nothing in flight past this point
 
   // normalise and store the valid rows
 #pragma unroll
@@ -285,40 +283,40 @@ __global__ void __launch_bounds__(kThreads) attn_mma_kernel(const MmaParams p) {
       __nv_bfloat16 *dst = p.out + (q_row0 + row) * stride + h * D + 2 * t4;
 #pragma unroll
       for (int i = 0; i < D / 8; ++i) {
-        *reinterpret_cast<uint32_t *>(dst + i * 8) = pack_bf16(o[i][2 * r] * inv, o[i][2 * r + 1] * inv);
+        *reinterpret_cast<uint32_t *>(dst + i * 8) =
+            pack_bf16(o[i][2 * r] * inv, o[i][2 * r + 1] * inv);
       }
     }
   }
 }
 
-template <int D, bool kBW>
-cudaError_t launch_mma(const MmaParams &p, dim3 grid, cudaStream_t stream) {
-  const int smem = (kBr + 4 * kBc) * D * 2;
-  cudaError_t e = cudaFuncSetAttribute(attn_mma_kernel<D, kBW>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+template <int D>
+cudaError_t launch_bw(const BwParams &p, dim3 grid, cudaStream_t stream) {
+  const int smem = (kBr + 2 * kStages * kBc) * D * 2;
+  static unsigned long long configured = 0;
+  cudaError_t e = set_smem_once(reinterpret_cast<const void *>(block_window_kernel<D>), smem,
+                                configured);
   if (e != cudaSuccess) return e;
-  attn_mma_kernel<D, kBW><<<grid, kThreads, smem, stream>>>(p);
+  block_window_kernel<D><<<grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_block_window_attn(const BlockWindowArgs &a, cudaStream_t stream) {
-  MmaParams p{};
+  BwParams p{};
   p.q = static_cast<const __nv_bfloat16 *>(a.q);
   p.k = static_cast<const __nv_bfloat16 *>(a.k);
   p.v = static_cast<const __nv_bfloat16 *>(a.v);
   p.out = static_cast<__nv_bfloat16 *>(a.out);
   p.row_stride = static_cast<int64_t>(a.H) * a.D;
   p.scale_log2 = a.scale * 1.4426950408889634f;
-  p.H = a.H;
   p.n = a.n;
   p.block = a.block;
   p.look_back = a.look_back;
   p.look_ahead = a.look_ahead;
-  p.status = a.status;
   dim3 grid((a.n + kBr - 1) / kBr, a.H, a.batch);
-  return a.D == 64 ? launch_mma<64, true>(p, grid, stream) : launch_mma<128, true>(p, grid, stream);
+  return a.D == 64 ? launch_bw<64>(p, grid, stream) : launch_bw<128>(p, grid, stream);
 }
 
 }  // namespace pa

@@ -560,8 +560,10 @@ cudaError_t launch_tc(const VarlenArgs &a, cudaStream_t stream) {
   p.scale_log2 = a.scale * 1.4426950408889634f;
   p.status = a.status;
   const int smem = Cfg<D, kSlots, kMaxSeqs>::kSmemBytes;
-  cudaError_t e = cudaFuncSetAttribute(varlen_attn_tc_kernel<D, kSlots, kMaxSeqs>,
-                                       cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  static unsigned long long configured = 0;
+  cudaError_t e = set_smem_once(
+      reinterpret_cast<const void *>(varlen_attn_tc_kernel<D, kSlots, kMaxSeqs>), smem,
+      configured);
   if (e != cudaSuccess) return e;
   varlen_attn_tc_kernel<D, kSlots, kMaxSeqs><<<a.num_sms, kThreads, smem, stream>>>(mq, mk, mv, p);
   return cudaGetLastError();

@@ -29,6 +29,20 @@ struct BlockWindowArgs {
   int num_sms;
 };
 
+// Raises a kernel's dynamic shared-memory limit once per device (the
+// attribute persists; setting it on every launch costs host time between
+// back-to-back launches).  `done` is the caller's per-kernel device bitmask.
+inline cudaError_t set_smem_once(const void *kernel, int smem, unsigned long long &done) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = 1ull << (dev & 63);
+  if (__atomic_load_n(&done, __ATOMIC_ACQUIRE) & bit) return cudaSuccess;
+  e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+  if (e == cudaSuccess) __atomic_fetch_or(&done, bit, __ATOMIC_ACQ_REL);
+  return e;
+}
+
 // Launchers: return cudaSuccess or the launch error.
 cudaError_t launch_varlen_attn(const VarlenArgs &a, cudaStream_t stream);
 cudaError_t launch_block_window_attn(const BlockWindowArgs &a, cudaStream_t stream);

@@ -49,10 +49,10 @@ def test_token2wav_config(pv, n, look):
     assert pv.get_device_status() == 0
 
 
-@pytest.mark.parametrize("block,D", [(1, 64), (7, 128), (64, 64), (200, 128)])
+@pytest.mark.parametrize("block,D", [(1, 64), (7, 128), (64, 64), (200, 128), (24, 128), (13, 64)])
 def test_other_blocks_and_head_dims(pv, block, D):
     w = workloads.random_block_window(2, 333, 3, D, block, seed=block + D)
-    for lb, la in [(0, 0), (1, 2)]:
+    for lb, la in [(0, 0), (1, 2), (4, 0)]:
         got = oracle.to_f64(_run(pv, w, lb, la))
         want = oracle.block_window_attention(w.q, w.k, w.v, block, lb, la, w.scale)
         assert_close_to_oracle(got, want, f"block={block} D={D} look=({lb},{la})")

@@ -68,7 +68,7 @@ def test_max_batch(pv):
 
 def test_scale_argument(pv):
     w = workloads.random_varlen([150, 40], None, 2, 128, seed=11)
-    for scale in (0.0, 0.02, 0.3):
+    for scale in (0.0, 0.02, 0.3, -0.1):   # negative: the scaled-first softmax path
         out, _, _ = gpu_varlen(pv, w, scale=scale)
         cu = oracle.cu_seqlens_from_lengths(w.lengths_q)
         want = oracle.varlen_attention(w.q, w.k, w.v, cu, cu, scale)
