@@ -19,11 +19,16 @@ the integer steps), written for a reader to check against the definitions:
   Purpose and Change).
 * ``work_order``: the length-ordered enumeration of (sequence, head, q-tile)
   work items.
+* ``cfg_combine``: segment-aware unpack of each request's image span with the
+  per-request classifier-free-guidance combine ("feat: Support dynamic
+  batching for heterogeneous diffusion requests", CFG behavior).
 
-Every function is pinned by tests in ``tests/test_oracle_pins.py`` against
+Every function is pinned by tests in ``tests/test_oracle_pins.py`` and
+``tests/test_oracle_cfg.py`` against
 brute force, closed forms, a library routine and the pages' invariants.
 """
 from .packing import cu_seqlens_from_lengths, pack, unpack, work_order
+from .cfg import cfg_combine
 from .attention import (
     masked_attention,
     varlen_mask,
@@ -40,5 +45,5 @@ __all__ = [
     "cu_seqlens_from_lengths", "pack", "unpack", "work_order",
     "masked_attention", "varlen_mask", "varlen_attention", "key_padding_attention",
     "block_window_mask", "block_window_attention", "to_f64",
-    "varlen_useful_flops", "block_window_useful_flops",
+    "varlen_useful_flops", "block_window_useful_flops", "cfg_combine",
 ]
