@@ -432,6 +432,8 @@ def run_attn_only(args):
     pv.get_device_status()
     if args.workload == "token2wav":
         return run_block_window_only(args, dev)
+    if args.workload.startswith("cfg_combine"):
+        return run_cfg_combine_only(args, dev)
     if args.workload in workloads.VARLEN_CONFIGS:
         w = workloads.VARLEN_CONFIGS[args.workload]()
     else:
@@ -539,6 +541,46 @@ def run_e2e(pv, pw, L, dev, scale, steps, want_out):
     return e0.elapsed_time(e1) / steps, h2d, d2h
 
 
+def run_cfg_combine_only(args, dev):
+    """Segment-aware unpack + CFG combine alone on the CFG batch's layout
+    (cfg_combine: rows of 64 channels; cfg_combine_3072: attention-output rows
+    of 24 x 128).  Reports us per launch and HBM GB/s of the algorithmic bytes
+    (positive and negative image rows read once, output rows written once)."""
+    import packed_varlen_gb300 as pv
+    C = 3072 if args.workload.endswith("3072") else 64
+    seg = workloads.cfg_segments(C=C)
+    i32 = lambda x: torch.tensor(x, dtype=torch.int32, device=dev)
+    cu = pv.cu_seqlens_from_lengths(i32(seg.lengths))
+    flat = seg.flat.to(dev)
+    args_t = (i32(seg.text), i32(seg.pos_seq), i32(seg.neg_seq),
+              torch.tensor(seg.cfg_scale, device=dev), i32(seg.cfg_normalize))
+    out = torch.zeros((len(seg.pos_seq), seg.img_max, C), dtype=torch.bfloat16, device=dev)
+    n_img = [seg.lengths[p] - seg.text[p] for p in seg.pos_seq]
+    nbytes = sum(n * C * 2 * (3 if q >= 0 else 2) for n, q in zip(n_img, seg.neg_seq))
+    flusher = L2Flusher(dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(args.warmup):
+        pv.cfg_combine(flat, cu, *args_t, seg.img_max, out=out)
+    ts = []
+    for _ in range(args.steps):
+        flusher.flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        pv.cfg_combine(flat, cu, *args_t, seg.img_max, out=out)
+        e1.record(stream)
+        ts.append((e0, e1))
+    torch.cuda.synchronize()
+    if pv.get_device_status() != 0:
+        raise RuntimeError("device status error")
+    us = 1e3 * statistics.median(a.elapsed_time(b) for a, b in ts)
+    peaks, src = _peaks()
+    gbs = nbytes / (us * 1e-6) / 1e9
+    print(json.dumps({"workload": args.workload, "row_elems": C, "requests": len(n_img),
+                      "image_rows": sum(n_img), "bytes": nbytes, "us": us, "gbs": gbs,
+                      "hbm_frac": gbs / peaks["hbm_gbs"], "peak_source": src}), flush=True)
+    return 0
+
+
 def run_block_window_only(args, dev):
     """Block-window layers alone (profiling): median us per layer type with a
     clean L2 before each launch, and a one-CTA kernel for the launch floor."""
@@ -585,7 +627,8 @@ def main():
     ap.add_argument("--attn-only", action="store_true",
                     help="time the attention kernel alone (profiling); not the bench line")
     ap.add_argument("--workload", default="single_8k",
-                    help="with --attn-only: a varlen config name or single_<N>k")
+                    help="with --attn-only: a varlen config name, single_<N>k, token2wav, "
+                         "cfg_combine or cfg_combine_3072")
     args = ap.parse_args()
     if args.attn_only:
         return run_attn_only(args)

@@ -53,6 +53,8 @@ typedef enum {
                                         pa_cu_seqlens_from_lengths */
 #define PA_DEVICE_ERR_CAPACITY 5     /* pa_varlen_work_order: more items than capacity */
 #define PA_DEVICE_ERR_SMEM_ALIGN 6   /* dynamic shared memory not 1024-byte aligned (kernel skipped) */
+#define PA_DEVICE_ERR_SEGMENT 7      /* pa_cfg_combine: bad sequence index, image offset or
+                                        mismatched positive/negative image spans */
 
 /* Largest batch (number of packed sequences) the attention kernels accept. */
 #define PA_MAX_BATCH 1024
@@ -150,6 +152,39 @@ pa_status pa_pack(const void *padded, void *flat, const int32_t *cu, int32_t bat
  */
 pa_status pa_unpack(const void *flat, void *padded, const int32_t *cu, int32_t batch,
                     int32_t s_max, int32_t total, int64_t row_bytes, pa_stream_t stream);
+
+/*
+ * pa_cfg_combine -- segment-aware unpack of each request's image span with
+ * the per-request classifier-free-guidance combine.
+ *
+ * Defined by "feat: Support dynamic batching for heterogeneous diffusion
+ * requests" (AttentionSegment: text / image / negative-text spans used to
+ * scatter outputs back to request-local state; CFG behavior: after the
+ * per-request split, out = negative + true_cfg_scale * (positive - negative),
+ * with true_cfg_scale and cfg_normalize per request).  Request r's positive
+ * pass is packed sequence pos_seq[r], its negative pass sequence neg_seq[r]
+ * (< 0: no CFG, the positive image rows are copied).  The image span of
+ * sequence b is rows [cu[b] + img_off[b], cu[b+1]) of `flat`.  With
+ * cfg_normalize[r] != 0 each combined row is rescaled to the L2 norm of its
+ * positive row (rows whose combined norm is 0 are written as 0).
+ *
+ * flat [total, row_elems] bf16; out [requests, img_max, row_elems] bf16:
+ * rows [0, n_img(r)) of slot r are written, the others left untouched.
+ * cu device int32 [batch + 1]; img_off device int32 [batch]; pos_seq,
+ * neg_seq, cfg_normalize device int32 [requests]; cfg_scale device float
+ * [requests].  Arithmetic in fp32, output rounded to bf16.
+ * batch in [1, 65535], requests in [1, 65535], total >= 0, img_max >= 0,
+ * row_elems a positive multiple of 8; flat and out 16-byte aligned.
+ * A request with an out-of-range sequence or image offset, positive and
+ * negative image spans of different lengths, or more than img_max image
+ * rows records PA_DEVICE_ERR_SEGMENT and is skipped.
+ */
+pa_status pa_cfg_combine(const void *flat, void *out, const int32_t *cu,
+                         const int32_t *img_off, const int32_t *pos_seq,
+                         const int32_t *neg_seq, const float *cfg_scale,
+                         const int32_t *cfg_normalize, int32_t batch, int32_t requests,
+                         int32_t total, int32_t img_max, int32_t row_elems,
+                         pa_stream_t stream);
 
 /*
  * pa_varlen_num_work_items -- host-side count of attention work items,

@@ -24,7 +24,8 @@ STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED",
                 3: "PA_ERR_MISALIGNED", 4: "PA_ERR_CUDA", 5: "PA_ERR_DEVICE"}
 DEVICE_ERRORS = {0: "PA_DEVICE_OK", 1: "PA_DEVICE_ERR_CU_SEQLENS", 2: "PA_DEVICE_ERR_MAX_LEN",
                  3: "PA_DEVICE_ERR_TIMEOUT", 4: "PA_DEVICE_ERR_LENGTH",
-                 5: "PA_DEVICE_ERR_CAPACITY", 6: "PA_DEVICE_ERR_SMEM_ALIGN"}
+                 5: "PA_DEVICE_ERR_CAPACITY", 6: "PA_DEVICE_ERR_SMEM_ALIGN",
+                 7: "PA_DEVICE_ERR_SEGMENT"}
 MAX_BATCH = 1024
 VARLEN_TILE_M = 256
 
@@ -56,6 +57,7 @@ _SIGNATURES = {
     "pa_status_string": ([_c_i32], ctypes.c_char_p),
     "pa_selftest_wait_timeout": ([_c_i32, _c_ptr], _c_i32),
     "pa_last_cuda_error": ([], ctypes.c_char_p),
+    "pa_cfg_combine": ([_c_ptr] * 8 + [_c_i32] * 5 + [_c_ptr], _c_i32),
 }
 
 
@@ -223,6 +225,40 @@ def unpack(flat: torch.Tensor, cu_seqlens: torch.Tensor, padded_out: torch.Tenso
                        flat.shape[0], _row_bytes(flat, 1), _stream(stream))
     _check("pa_unpack", st)
     return padded_out
+
+
+def cfg_combine(flat: torch.Tensor, cu_seqlens: torch.Tensor, img_off: torch.Tensor,
+                pos_seq: torch.Tensor, neg_seq: torch.Tensor, cfg_scale: torch.Tensor,
+                cfg_normalize: torch.Tensor, img_max: int, out: Optional[torch.Tensor] = None,
+                stream=None) -> torch.Tensor:
+    """Per-request image-span unpack with the CFG combine (pa_cfg_combine).
+    flat [T, ...] bf16 -> out [R, img_max, ...] bf16; index tensors int32 and
+    cfg_scale float32 on the device.  Rows of ``out`` past each request's
+    image span are left as they are (a fresh ``out`` is zero-filled)."""
+    lib = load_library()
+    _need(flat, "flat", torch.bfloat16)
+    _need(cu_seqlens, "cu_seqlens", torch.int32, 1)
+    for t, n in ((img_off, "img_off"), (pos_seq, "pos_seq"), (neg_seq, "neg_seq"),
+                 (cfg_normalize, "cfg_normalize")):
+        _need(t, n, torch.int32, 1)
+    _need(cfg_scale, "cfg_scale", torch.float32, 1)
+    B, R = cu_seqlens.numel() - 1, pos_seq.numel()
+    if img_off.numel() != B or neg_seq.numel() != R or cfg_scale.numel() != R or \
+            cfg_normalize.numel() != R:
+        raise ValueError("segment metadata sizes do not match")
+    row = _row_bytes(flat, 1) // 2
+    if out is None:
+        out = torch.zeros((R, int(img_max)) + tuple(flat.shape[1:]), dtype=torch.bfloat16,
+                          device=flat.device)
+    _need(out, "out", torch.bfloat16)
+    if out.shape[0] != R or out.shape[1] != img_max or out.shape[2:] != flat.shape[1:]:
+        raise ValueError("out must be [R, img_max, *flat.shape[1:]]")
+    st = lib.pa_cfg_combine(flat.data_ptr(), out.data_ptr(), cu_seqlens.data_ptr(),
+                            img_off.data_ptr(), pos_seq.data_ptr(), neg_seq.data_ptr(),
+                            cfg_scale.data_ptr(), cfg_normalize.data_ptr(), B, R, flat.shape[0],
+                            int(img_max), row, _stream(stream))
+    _check("pa_cfg_combine", st)
+    return out
 
 
 def varlen_num_work_items(cu_seqlens_q_host, H: int, tile_m: int = VARLEN_TILE_M) -> int:

@@ -19,6 +19,8 @@ constexpr int kMaxDevices = 64;
 int32_t *g_status_addr[kMaxDevices];
 int g_num_sms[kMaxDevices];
 
+}  // namespace
+
 // Device address of the status word and SM count of the current device.
 cudaError_t device_context(int32_t **status, int *num_sms) {
   int dev = 0;
@@ -39,6 +41,8 @@ cudaError_t device_context(int32_t **status, int *num_sms) {
   *num_sms = g_num_sms[dev];
   return cudaSuccess;
 }
+
+namespace {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 bool aligned4(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 3u) == 0; }
@@ -169,6 +173,10 @@ __global__ void wait_timeout_kernel(long long limit_cycles, int32_t *status) {
                      limit_cycles);
 }
 
+
+
+}  // namespace
+
 // Last CUDA error this thread saw inside the library (for pa_last_cuda_error).
 thread_local cudaError_t t_last_cuda_error = cudaSuccess;
 
@@ -178,7 +186,6 @@ pa_status from_cuda(cudaError_t e) {
   return PA_ERR_CUDA;
 }
 
-}  // namespace
 }  // namespace pa
 
 using namespace pa;

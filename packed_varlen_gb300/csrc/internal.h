@@ -43,6 +43,13 @@ inline cudaError_t set_smem_once(const void *kernel, int smem, unsigned long lon
   return e;
 }
 
+// Device address of the per-device status word and the SM count of the
+// current device (api.cu).
+cudaError_t device_context(int32_t **status, int *num_sms);
+
+// Maps a CUDA error to a pa_status and remembers it for pa_last_cuda_error.
+pa_status from_cuda(cudaError_t e);
+
 // Launchers: return cudaSuccess or the launch error.
 cudaError_t launch_varlen_attn(const VarlenArgs &a, cudaStream_t stream);
 cudaError_t launch_block_window_attn(const BlockWindowArgs &a, cudaStream_t stream);

@@ -30,7 +30,8 @@ def test_header_declares_expected_entry_points():
     names = _declared()
     for n in ["pa_varlen_attn_fwd", "pa_block_window_attn_fwd", "pa_cu_seqlens_from_lengths",
               "pa_pack", "pa_unpack", "pa_varlen_work_order", "pa_varlen_num_work_items",
-              "pa_get_device_status", "pa_status_string"]:
+              "pa_get_device_status", "pa_status_string", "pa_cfg_combine",
+              "pa_last_cuda_error", "pa_selftest_wait_timeout"]:
         assert n in names
 
 
@@ -110,3 +111,18 @@ def test_num_work_items_matches_oracle(lib):
         for H in (1, 24):
             for tile in (128, pv.VARLEN_TILE_M):
                 assert pv.varlen_num_work_items(cu, H, tile) == len(oracle.work_order(L, L, H, tile))
+
+
+def test_cfg_combine_host_checks(lib):
+    # a template of arguments that is only ever passed with one field broken
+    args = [A] * 8 + [4, 2, 100, 50, 64, None]
+    bad = list(args); bad[0] = None
+    assert lib.pa_cfg_combine(*bad) == 1
+    bad = list(args); bad[8] = 0
+    assert lib.pa_cfg_combine(*bad) == 1
+    bad = list(args); bad[12] = 60   # row_elems not a multiple of 8
+    assert lib.pa_cfg_combine(*bad) == 3
+    bad = list(args); bad[1] = MIS
+    assert lib.pa_cfg_combine(*bad) == 3
+    bad = list(args); bad[9] = 70000
+    assert lib.pa_cfg_combine(*bad) == 2

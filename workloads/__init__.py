@@ -128,10 +128,12 @@ def lengths_single_edit() -> List[int]:
     return [256 + 2 * 16384]
 
 
-def lengths_cfg_batch(g: torch.Generator) -> Tuple[List[int], List[int]]:
+def lengths_cfg_batch_detail(g: torch.Generator) -> Tuple[List[int], List[int], List[int]]:
     """Eight requests, image tokens chosen uniformly from IMAGE_TOKENS; each
     becomes two sequences (positive text + image, negative text + image) with
-    independent text lengths ~ U[8, 256].  Returns (lengths, request index)."""
+    independent text lengths ~ U[8, 256].  Returns (lengths, request index,
+    text lengths); sequence 2r is request r's positive pass, 2r + 1 its
+    negative pass."""
     img_idx = torch.randint(0, len(IMAGE_TOKENS), (8,), generator=g).tolist()
     text = torch.randint(8, 257, (16,), generator=g).tolist()
     lengths, owner = [], []
@@ -139,6 +141,12 @@ def lengths_cfg_batch(g: torch.Generator) -> Tuple[List[int], List[int]]:
         for s in range(2):
             lengths.append(text[2 * r + s] + IMAGE_TOKENS[img_idx[r]])
             owner.append(r)
+    return lengths, owner, text
+
+
+def lengths_cfg_batch(g: torch.Generator) -> Tuple[List[int], List[int]]:
+    """(lengths, request index) of the CFG batch; see lengths_cfg_batch_detail."""
+    lengths, owner, _ = lengths_cfg_batch_detail(g)
     return lengths, owner
 
 
@@ -243,3 +251,37 @@ VARLEN_CONFIGS = {
     "single_edit": single_edit,
     "cfg_dynamic_batch": cfg_batch,
 }
+
+
+@dataclass
+class CfgSegments:
+    """Model output rows of a CFG-doubled packed batch and its segment layout:
+    flat [sum(lengths), C]; sequence b holds text rows [0, text[b]) then image
+    rows; request r's positive pass is pos_seq[r], its negative pass
+    neg_seq[r] (-1: no CFG); per-request guidance scale and normalize flag."""
+    lengths: List[int]
+    text: List[int]
+    pos_seq: List[int]
+    neg_seq: List[int]
+    cfg_scale: List[float]
+    cfg_normalize: List[int]
+    flat: torch.Tensor
+    img_max: int
+
+
+def cfg_segments(C: int = 64, seed: int = 5, scales=(2.0, 7.0), normalize_every: int = 0
+                 ) -> CfgSegments:
+    """The CFG dynamic batch's lengths (drawn as in cfg_batch) with bf16
+    N(0, 1) rows of width C drawn after them; request r uses guidance scale
+    scales[r % len(scales)] (the page's example pair 2.0 / 7.0 by default) and
+    normalizes when normalize_every > 0 and r % normalize_every == 0."""
+    g = torch.Generator().manual_seed(seed)
+    L, owner, text = lengths_cfg_batch_detail(g)
+    flat = _randn_bf16(g, (sum(L), C))
+    R = len(L) // 2
+    img = [L[2 * r] - text[2 * r] for r in range(R)]
+    return CfgSegments(L, text, [2 * r for r in range(R)], [2 * r + 1 for r in range(R)],
+                       [float(scales[r % len(scales)]) for r in range(R)],
+                       [1 if normalize_every and r % normalize_every == 0 else 0
+                        for r in range(R)],
+                       flat, max(img))
