@@ -363,6 +363,7 @@ def run_ours(args):
 
     if pv.get_device_status() != 0:
         raise RuntimeError("device status error during the timed run")
+    cfg_meas = measure_cfg_combine(dev, 3072, 10, 3)
 
     peaks, peak_src = _peaks()
     attn_mean_ms = statistics.mean(attn_ms)
@@ -414,6 +415,7 @@ def run_ours(args):
                 / peaks["hbm_gbs"],
                 "useful_tflops": bw_flops / (total_bw_us * 1e-6) / 1e12,
                 "launches": len(bw.layers)},
+            "cfg_combine": cfg_meas,
         }
         print(json.dumps(result), flush=True)
     if dist:
@@ -541,13 +543,12 @@ def run_e2e(pv, pw, L, dev, scale, steps, want_out):
     return e0.elapsed_time(e1) / steps, h2d, d2h
 
 
-def run_cfg_combine_only(args, dev):
-    """Segment-aware unpack + CFG combine alone on the CFG batch's layout
-    (cfg_combine: rows of 64 channels; cfg_combine_3072: attention-output rows
-    of 24 x 128).  Reports us per launch and HBM GB/s of the algorithmic bytes
-    (positive and negative image rows read once, output rows written once)."""
+def measure_cfg_combine(dev, C, steps, warmup):
+    """Segment-aware unpack + CFG combine alone on the CFG batch's layout with
+    rows of C channels (64: latent channels, 3072: 24 x 128 attention output).
+    Returns us per launch and HBM GB/s of the algorithmic bytes (positive and
+    negative image rows read once, output rows written once)."""
     import packed_varlen_gb300 as pv
-    C = 3072 if args.workload.endswith("3072") else 64
     seg = workloads.cfg_segments(C=C)
     i32 = lambda x: torch.tensor(x, dtype=torch.int32, device=dev)
     cu = pv.cu_seqlens_from_lengths(i32(seg.lengths))
@@ -559,10 +560,10 @@ def run_cfg_combine_only(args, dev):
     nbytes = sum(n * C * 2 * (3 if q >= 0 else 2) for n, q in zip(n_img, seg.neg_seq))
     flusher = L2Flusher(dev)
     stream = torch.cuda.current_stream()
-    for _ in range(args.warmup):
+    for _ in range(warmup):
         pv.cfg_combine(flat, cu, *args_t, seg.img_max, out=out)
     ts = []
-    for _ in range(args.steps):
+    for _ in range(steps):
         flusher.flush()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
@@ -575,9 +576,15 @@ def run_cfg_combine_only(args, dev):
     us = 1e3 * statistics.median(a.elapsed_time(b) for a, b in ts)
     peaks, src = _peaks()
     gbs = nbytes / (us * 1e-6) / 1e9
-    print(json.dumps({"workload": args.workload, "row_elems": C, "requests": len(n_img),
-                      "image_rows": sum(n_img), "bytes": nbytes, "us": us, "gbs": gbs,
-                      "hbm_frac": gbs / peaks["hbm_gbs"], "peak_source": src}), flush=True)
+    return {"workload": f"cfg dynamic batch, {len(n_img)} requests x (positive, negative), "
+                        f"rows of {C} bf16", "image_rows": sum(n_img), "bytes": nbytes,
+            "us": us, "gbs": gbs, "hbm_frac": gbs / peaks["hbm_gbs"], "peak_source": src}
+
+
+def run_cfg_combine_only(args, dev):
+    C = 3072 if args.workload.endswith("3072") else 64
+    print(json.dumps(dict(measure_cfg_combine(dev, C, args.steps, args.warmup),
+                          workload_name=args.workload)), flush=True)
     return 0
 
 

@@ -19,16 +19,19 @@ the integer steps), written for a reader to check against the definitions:
   Purpose and Change).
 * ``work_order``: the length-ordered enumeration of (sequence, head, q-tile)
   work items.
+* ``rope``, ``rope_positions``: rotary embedding with request-local
+  positions ("feat: Support dynamic batching ...", Correctness model).
 * ``cfg_combine``: segment-aware unpack of each request's image span with the
   per-request classifier-free-guidance combine ("feat: Support dynamic
   batching for heterogeneous diffusion requests", CFG behavior).
 
 Every function is pinned by tests in ``tests/test_oracle_pins.py`` and
-``tests/test_oracle_cfg.py`` against
+``tests/test_oracle_cfg.py`` and ``tests/test_oracle_rope.py`` against
 brute force, closed forms, a library routine and the pages' invariants.
 """
 from .packing import cu_seqlens_from_lengths, pack, unpack, work_order
 from .cfg import cfg_combine
+from .rope import rope, rope_positions
 from .attention import (
     masked_attention,
     varlen_mask,
@@ -45,5 +48,5 @@ __all__ = [
     "cu_seqlens_from_lengths", "pack", "unpack", "work_order",
     "masked_attention", "varlen_mask", "varlen_attention", "key_padding_attention",
     "block_window_mask", "block_window_attention", "to_f64",
-    "varlen_useful_flops", "block_window_useful_flops", "cfg_combine",
+    "varlen_useful_flops", "block_window_useful_flops", "cfg_combine", "rope", "rope_positions",
 ]
