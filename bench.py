@@ -364,6 +364,7 @@ def run_ours(args):
     if pv.get_device_status() != 0:
         raise RuntimeError("device status error during the timed run")
     cfg_meas = measure_cfg_combine(dev, 3072, 10, 3)
+    rope_meas = measure_rope(dev, 10, 3)
 
     peaks, peak_src = _peaks()
     attn_mean_ms = statistics.mean(attn_ms)
@@ -416,6 +417,7 @@ def run_ours(args):
                 "useful_tflops": bw_flops / (total_bw_us * 1e-6) / 1e12,
                 "launches": len(bw.layers)},
             "cfg_combine": cfg_meas,
+            "rope": rope_meas,
         }
         print(json.dumps(result), flush=True)
     if dist:
@@ -436,6 +438,9 @@ def run_attn_only(args):
         return run_block_window_only(args, dev)
     if args.workload.startswith("cfg_combine"):
         return run_cfg_combine_only(args, dev)
+    if args.workload == "rope":
+        print(json.dumps(measure_rope(dev, args.steps, args.warmup)), flush=True)
+        return 0
     if args.workload in workloads.VARLEN_CONFIGS:
         w = workloads.VARLEN_CONFIGS[args.workload]()
     else:
@@ -581,6 +586,37 @@ def measure_cfg_combine(dev, C, steps, warmup):
             "us": us, "gbs": gbs, "hbm_frac": gbs / peaks["hbm_gbs"], "peak_source": src}
 
 
+def measure_rope(dev, steps, warmup):
+    """Request-local RoPE alone on the mixed-resolution batch's q and k (in
+    place).  Algorithmic bytes: q and k read once and written once."""
+    import packed_varlen_gb300 as pv
+    w = workloads.mixed_res()
+    q, k = w.q.to(dev), w.k.to(dev)
+    cu = pv.cu_seqlens_from_lengths(torch.tensor(w.lengths_q, dtype=torch.int32, device=dev))
+    nbytes = 2 * 2 * q.numel() * 2
+    flusher = L2Flusher(dev)
+    stream = torch.cuda.current_stream()
+    for _ in range(warmup):
+        pv.rope_packed(q, k, cu, cu)
+    ts = []
+    for _ in range(steps):
+        flusher.flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        pv.rope_packed(q, k, cu, cu)
+        e1.record(stream)
+        ts.append((e0, e1))
+    torch.cuda.synchronize()
+    if pv.get_device_status() != 0:
+        raise RuntimeError("device status error")
+    us = 1e3 * statistics.median(a.elapsed_time(b) for a, b in ts)
+    peaks, src = _peaks()
+    gbs = nbytes / (us * 1e-6) / 1e9
+    return {"workload": "mixed-resolution batch q and k, T=%d, H=24, D=128, in place" % q.shape[0],
+            "bytes": nbytes, "us": us, "gbs": gbs, "hbm_frac": gbs / peaks["hbm_gbs"],
+            "peak_source": src}
+
+
 def run_cfg_combine_only(args, dev):
     C = 3072 if args.workload.endswith("3072") else 64
     print(json.dumps(dict(measure_cfg_combine(dev, C, args.steps, args.warmup),
@@ -635,7 +671,7 @@ def main():
                     help="time the attention kernel alone (profiling); not the bench line")
     ap.add_argument("--workload", default="single_8k",
                     help="with --attn-only: a varlen config name, single_<N>k, token2wav, "
-                         "cfg_combine or cfg_combine_3072")
+                         "cfg_combine, cfg_combine_3072 or rope")
     args = ap.parse_args()
     if args.attn_only:
         return run_attn_only(args)

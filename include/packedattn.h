@@ -154,6 +154,33 @@ pa_status pa_unpack(const void *flat, void *padded, const int32_t *cu, int32_t b
                     int32_t s_max, int32_t total, int64_t row_bytes, pa_stream_t stream);
 
 /*
+ * pa_rope_packed -- rotary position embedding on packed q and k, in place,
+ * with request-local positions.
+ *
+ * The dynamic path rebuilds RoPE per request from request-local state and
+ * never infers positions from packed global offsets, so a request gets the
+ * same RoPE alone or inside a mixed batch ("feat: Support dynamic batching
+ * for heterogeneous diffusion requests", Correctness model).  The pages give
+ * no formula; this is the rotary embedding of Su et al. (RoFormer) on
+ * interleaved pairs: token j of sequence b sits at position
+ * p = pos_offset[b] + j and every head's pair (x_2i, x_2i+1) is rotated by the
+ * angle p * base^(-2i/D).  Angles are reduced exactly (double-precision
+ * fraction of a turn), sin/cos and the rotation in fp32, output bf16.
+ *
+ * q [total_q, H, D] and k [total_k, H, D] bf16 are updated in place at the
+ * rows of their sequences (rows past cu[batch] are left untouched).
+ * cu_seqlens_q / cu_seqlens_k: device int32 [batch + 1]; pos_offset: device
+ * int32 [batch] or NULL (all zero).  batch in [1, 65535], H >= 1, D even,
+ * a multiple of 8 and at most 512, base finite and > 0; q, k 16-byte
+ * aligned.  Bad boundaries record PA_DEVICE_ERR_CU_SEQLENS; the sequence is
+ * skipped.
+ */
+pa_status pa_rope_packed(void *q, void *k, const int32_t *cu_seqlens_q,
+                         const int32_t *cu_seqlens_k, const int32_t *pos_offset,
+                         int32_t batch, int32_t total_q, int32_t total_k, int32_t H,
+                         int32_t D, float base, pa_stream_t stream);
+
+/*
  * pa_cfg_combine -- segment-aware unpack of each request's image span with
  * the per-request classifier-free-guidance combine.
  *

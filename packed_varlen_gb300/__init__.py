@@ -58,6 +58,7 @@ _SIGNATURES = {
     "pa_selftest_wait_timeout": ([_c_i32, _c_ptr], _c_i32),
     "pa_last_cuda_error": ([], ctypes.c_char_p),
     "pa_cfg_combine": ([_c_ptr] * 8 + [_c_i32] * 5 + [_c_ptr], _c_i32),
+    "pa_rope_packed": ([_c_ptr] * 5 + [_c_i32] * 5 + [_c_f32, _c_ptr], _c_i32),
 }
 
 
@@ -225,6 +226,32 @@ def unpack(flat: torch.Tensor, cu_seqlens: torch.Tensor, padded_out: torch.Tenso
                        flat.shape[0], _row_bytes(flat, 1), _stream(stream))
     _check("pa_unpack", st)
     return padded_out
+
+
+def rope_packed(q: torch.Tensor, k: torch.Tensor, cu_seqlens_q: torch.Tensor,
+                cu_seqlens_k: torch.Tensor, pos_offset: Optional[torch.Tensor] = None,
+                base: float = 10000.0, stream=None):
+    """Rotary embedding with request-local positions, in place on packed q
+    [Tq, H, D] and k [Tk, H, D] bf16 (pa_rope_packed).  Returns (q, k)."""
+    lib = load_library()
+    _need(q, "q", torch.bfloat16, 3)
+    _need(k, "k", torch.bfloat16, 3)
+    _need(cu_seqlens_q, "cu_seqlens_q", torch.int32, 1)
+    _need(cu_seqlens_k, "cu_seqlens_k", torch.int32, 1)
+    if k.shape[1:] != q.shape[1:] or cu_seqlens_k.numel() != cu_seqlens_q.numel():
+        raise ValueError("q/k heads, dims or batch differ")
+    B = cu_seqlens_q.numel() - 1
+    ptr = None
+    if pos_offset is not None:
+        _need(pos_offset, "pos_offset", torch.int32, 1)
+        if pos_offset.numel() != B:
+            raise ValueError("pos_offset must have one entry per sequence")
+        ptr = pos_offset.data_ptr()
+    st = lib.pa_rope_packed(q.data_ptr(), k.data_ptr(), cu_seqlens_q.data_ptr(),
+                            cu_seqlens_k.data_ptr(), ptr, B, q.shape[0], k.shape[0], q.shape[1],
+                            q.shape[2], float(base), _stream(stream))
+    _check("pa_rope_packed", st)
+    return q, k
 
 
 def cfg_combine(flat: torch.Tensor, cu_seqlens: torch.Tensor, img_off: torch.Tensor,

@@ -31,7 +31,7 @@ def test_header_declares_expected_entry_points():
     for n in ["pa_varlen_attn_fwd", "pa_block_window_attn_fwd", "pa_cu_seqlens_from_lengths",
               "pa_pack", "pa_unpack", "pa_varlen_work_order", "pa_varlen_num_work_items",
               "pa_get_device_status", "pa_status_string", "pa_cfg_combine",
-              "pa_last_cuda_error", "pa_selftest_wait_timeout"]:
+              "pa_last_cuda_error", "pa_selftest_wait_timeout", "pa_rope_packed"]:
         assert n in names
 
 
@@ -126,3 +126,13 @@ def test_cfg_combine_host_checks(lib):
     assert lib.pa_cfg_combine(*bad) == 3
     bad = list(args); bad[9] = 70000
     assert lib.pa_cfg_combine(*bad) == 2
+
+
+def test_rope_host_checks(lib):
+    # every call has exactly one broken field, so nothing reaches the device
+    ok = [A, A, A, A, None, 2, 10, 10, 2, 64, 1e4, None]
+    for i, v, code in [(0, None, 1), (5, 0, 1), (9, 63, 1), (10, -1.0, 1), (10, math.inf, 1),
+                       (9, 520, 2), (9, 12, 2), (0, MIS, 3), (2, A + 2, 3), (4, A + 1, 3)]:
+        bad = list(ok)
+        bad[i] = v
+        assert lib.pa_rope_packed(*bad) == code, (i, v)
