@@ -6,7 +6,9 @@ image tokens, H=24, D=128, bf16 N(0,1)):
   cu_seqlens from lengths -> pack q, k, v (padded -> flat) -> varlen
   attention -> unpack the output (flat -> padded).
 The Token2Wav block-window variant (22 layers, n=2400, H=16, D=64, block 24)
-is timed in the same run and reported under "block_window".
+is timed in the same run and reported under "block_window", and its fp32
+form (the DiT's own dtype, classifier-free guidance as batch 2) under
+"block_window_f32".
 
 Rank 0 prints one JSON line.  Under torchrun each rank runs its own batch
 (seed + rank) on its own GPU; no data moves between ranks (weak scaling);
@@ -337,29 +339,9 @@ def run_ours(args):
     e2e_mean = max_over_ranks(e2e_mean, dist, dev)
     e2e_value = flops * ws / (e2e_mean * 1e-3) / 1e12
 
-    # ---- block-window variant (Token2Wav), timed per layer -------------------
-    bw = workloads.token2wav()
-    bq, bk, bv = bw.q.to(dev), bw.k.to(dev), bw.v.to(dev)
-    bo = torch.empty_like(bq)
-    for _ in range(3):
-        for lb, la in bw.layers:
-            pv.block_window_attn_fwd(bq, bk, bv, bw.block, lb, la, out=bo)
-    torch.cuda.synchronize()
-    per_layer = {}
-    for lb, la in sorted(set(bw.layers)):
-        ts = []
-        for _ in range(20):
-            flusher.flush()
-            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-            e0.record(stream)
-            pv.block_window_attn_fwd(bq, bk, bv, bw.block, lb, la, out=bo)
-            e1.record(stream)
-            ts.append((e0, e1))
-        torch.cuda.synchronize()
-        per_layer[(lb, la)] = statistics.median(a.elapsed_time(b) for a, b in ts)
-    bw_bytes = 4 * bq.numel() * 2   # q, k, v read once, out written once
-    total_bw_us = sum(per_layer[l] for l in bw.layers) * 1e3
-    bw_flops = sum(block_window_flops(bw.n, bw.H, bw.D, bw.block, lb, la) for lb, la in bw.layers)
+    # ---- block-window variants (Token2Wav), timed per layer ------------------
+    bw_meas = measure_block_window(pv, workloads.token2wav(), False, dev, flusher, stream)
+    bw32_meas = measure_block_window(pv, workloads.token2wav_f32(), True, dev, flusher, stream)
 
     if pv.get_device_status() != 0:
         raise RuntimeError("device status error during the timed run")
@@ -407,15 +389,11 @@ def run_ours(args):
                            "double-buffered, all steps inside the timed region"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
-            "block_window": {
-                "workload": "token2wav n=2400 H=16 D=64 block=24, 19 x (0,0) + 3 x (1,1) layers",
-                "us_per_layer": {f"{lb},{la}": 1e3 * ms for (lb, la), ms in per_layer.items()},
-                "us_all_layers": total_bw_us,
-                "gbs_own_block_layer": bw_bytes / (per_layer[(0, 0)] * 1e-3) / 1e9,
-                "hbm_frac_own_block_layer": bw_bytes / (per_layer[(0, 0)] * 1e-3) / 1e9
-                / peaks["hbm_gbs"],
-                "useful_tflops": bw_flops / (total_bw_us * 1e-6) / 1e12,
-                "launches": len(bw.layers)},
+            "block_window": dict(bw_meas, hbm_frac_own_block_layer=bw_meas["gbs_own_block_layer"]
+                                 / peaks["hbm_gbs"]),
+            "block_window_f32": dict(bw32_meas,
+                                     hbm_frac_own_block_layer=bw32_meas["gbs_own_block_layer"]
+                                     / peaks["hbm_gbs"]),
             "cfg_combine": cfg_meas,
             "rope": rope_meas,
         }
@@ -434,7 +412,7 @@ def run_attn_only(args):
     dev = torch.device("cuda", 0)
     pv.load_library()
     pv.get_device_status()
-    if args.workload == "token2wav":
+    if args.workload in ("token2wav", "token2wav_f32"):
         return run_block_window_only(args, dev)
     if args.workload.startswith("cfg_combine"):
         return run_cfg_combine_only(args, dev)
@@ -617,6 +595,45 @@ def measure_rope(dev, steps, warmup):
             "peak_source": src}
 
 
+def measure_block_window(pv, bw, f32, dev, flusher, stream, reps=20):
+    """Median time of each Token2Wav layer type with a clean L2 before every
+    launch; bytes = q, k, v read once and out written once."""
+    fn = pv.block_window_attn_fwd_f32 if f32 else pv.block_window_attn_fwd
+    bq, bk, bv = bw.q.to(dev), bw.k.to(dev), bw.v.to(dev)
+    bo = torch.empty_like(bq)
+    for _ in range(3):
+        for lb, la in bw.layers:
+            fn(bq, bk, bv, bw.block, lb, la, out=bo)
+    torch.cuda.synchronize()
+    per_layer = {}
+    for lb, la in sorted(set(bw.layers)):
+        ts = []
+        for _ in range(reps):
+            flusher.flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            fn(bq, bk, bv, bw.block, lb, la, out=bo)
+            e1.record(stream)
+            ts.append((e0, e1))
+        torch.cuda.synchronize()
+        per_layer[(lb, la)] = statistics.median(a.elapsed_time(b) for a, b in ts)
+    nbytes = 4 * bq.numel() * bq.element_size()
+    total_us = sum(per_layer[l] for l in bw.layers) * 1e3
+    flops = sum(block_window_flops(bw.n, bw.H, bw.D, bw.block, lb, la) * bw.batch
+                for lb, la in bw.layers)
+    n_own = sum(1 for l in bw.layers if l == (0, 0))
+    return {
+        "workload": f"token2wav {'fp32' if f32 else 'bf16'} batch={bw.batch} n={bw.n} "
+                    f"H={bw.H} D={bw.D} block={bw.block}, {n_own} x (0,0) + "
+                    f"{len(bw.layers) - n_own} x (1,1) layers",
+        "us_per_layer": {f"{lb},{la}": 1e3 * ms for (lb, la), ms in per_layer.items()},
+        "us_all_layers": total_us,
+        "bytes_per_layer": nbytes,
+        "gbs_own_block_layer": nbytes / (per_layer[(0, 0)] * 1e-3) / 1e9,
+        "useful_tflops": flops / (total_us * 1e-6) / 1e12,
+        "launches": len(bw.layers)}
+
+
 def run_cfg_combine_only(args, dev):
     C = 3072 if args.workload.endswith("3072") else 64
     print(json.dumps(dict(measure_cfg_combine(dev, C, args.steps, args.warmup),
@@ -628,7 +645,9 @@ def run_block_window_only(args, dev):
     """Block-window layers alone (profiling): median us per layer type with a
     clean L2 before each launch, and a one-CTA kernel for the launch floor."""
     import packed_varlen_gb300 as pv
-    bw = workloads.token2wav()
+    f32 = args.workload == "token2wav_f32"
+    bw = workloads.token2wav_f32() if f32 else workloads.token2wav()
+    fwd = pv.block_window_attn_fwd_f32 if f32 else pv.block_window_attn_fwd
     bq, bk, bv = bw.q.to(dev), bw.k.to(dev), bw.v.to(dev)
     bo = torch.empty_like(bq)
     flusher = L2Flusher(dev)
@@ -636,8 +655,8 @@ def run_block_window_only(args, dev):
     lens = torch.tensor([5, 7], dtype=torch.int32, device=dev)
     cu = torch.empty(3, dtype=torch.int32, device=dev)
     res = {}
-    cases = [("0,0", lambda: pv.block_window_attn_fwd(bq, bk, bv, 24, 0, 0, out=bo)),
-             ("1,1", lambda: pv.block_window_attn_fwd(bq, bk, bv, 24, 1, 1, out=bo)),
+    cases = [("0,0", lambda: fwd(bq, bk, bv, 24, 0, 0, out=bo)),
+             ("1,1", lambda: fwd(bq, bk, bv, 24, 1, 1, out=bo)),
              ("floor", lambda: pv.cu_seqlens_from_lengths(lens, out=cu))]
     for name, fn in cases:
         for _ in range(args.warmup):
@@ -652,7 +671,7 @@ def run_block_window_only(args, dev):
             ts.append((e0, e1))
         torch.cuda.synchronize()
         res[name] = 1e3 * statistics.median(a.elapsed_time(b) for a, b in ts)
-    print(json.dumps({"workload": "token2wav", "us": res}), flush=True)
+    print(json.dumps({"workload": args.workload, "us": res}), flush=True)
     return 0
 
 
@@ -670,7 +689,7 @@ def main():
     ap.add_argument("--attn-only", action="store_true",
                     help="time the attention kernel alone (profiling); not the bench line")
     ap.add_argument("--workload", default="single_8k",
-                    help="with --attn-only: a varlen config name, single_<N>k, token2wav, "
+                    help="with --attn-only: a varlen config name, single_<N>k, token2wav, token2wav_f32, "
                          "cfg_combine, cfg_combine_3072 or rope")
     args = ap.parse_args()
     if args.attn_only:

@@ -116,6 +116,23 @@ pa_status pa_block_window_attn_fwd(const void *q, const void *k, const void *v, 
                                    int32_t H, int32_t D, float scale, pa_stream_t stream);
 
 /*
+ * pa_block_window_attn_fwd_f32 -- the same block-local attention in fp32.
+ *
+ * The Token2Wav DiT runs in fp32 with classifier-free guidance as batch 2
+ * ("[Perf][Model] Use block-sparse attention in Qwen2.5-Omni Token2Wav DiT",
+ * Purpose), and its block-local result stayed within 6e-6 of the dense masked
+ * SDPA (Test Result).  The window rule and the argument rules are those of
+ * pa_block_window_attn_fwd; q, k, v, out are fp32 [batch, n, H, D]
+ * contiguous, 16-byte aligned, caller-owned; out must not overlap q, k or v.
+ * Every product and sum is IEEE fp32 (no tensor-core tf32), exponentials by
+ * expf, so the result is within a few fp32 roundings of the exact one.
+ */
+pa_status pa_block_window_attn_fwd_f32(const float *q, const float *k, const float *v,
+                                       float *out, int32_t batch, int32_t n, int32_t block,
+                                       int32_t look_back, int32_t look_ahead, int32_t H,
+                                       int32_t D, float scale, pa_stream_t stream);
+
+/*
  * pa_cu_seqlens_from_lengths -- cu[0] = 0, cu[b+1] = cu[b] + lengths[b].
  *
  * The flat path's boundaries come from each request's real token count

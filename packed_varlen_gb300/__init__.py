@@ -47,6 +47,7 @@ _c_f32 = ctypes.c_float
 _SIGNATURES = {
     "pa_varlen_attn_fwd": ([_c_ptr] * 6 + [_c_i32] * 7 + [_c_f32, _c_ptr], _c_i32),
     "pa_block_window_attn_fwd": ([_c_ptr] * 4 + [_c_i32] * 7 + [_c_f32, _c_ptr], _c_i32),
+    "pa_block_window_attn_fwd_f32": ([_c_ptr] * 4 + [_c_i32] * 7 + [_c_f32, _c_ptr], _c_i32),
     "pa_cu_seqlens_from_lengths": ([_c_ptr, _c_ptr, _c_i32, _c_ptr], _c_i32),
     "pa_pack": ([_c_ptr, _c_ptr, _c_ptr, _c_i32, _c_i32, _c_i32, _c_i64, _c_ptr], _c_i32),
     "pa_unpack": ([_c_ptr, _c_ptr, _c_ptr, _c_i32, _c_i32, _c_i32, _c_i64, _c_ptr], _c_i32),
@@ -163,6 +164,31 @@ def block_window_attn_fwd(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, blo
                                       batch, n, int(block), int(look_back), int(look_ahead),
                                       H, D, float(scale), _stream(stream))
     _check("pa_block_window_attn_fwd", st)
+    return out
+
+
+def block_window_attn_fwd_f32(q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, block: int,
+                              look_back: int, look_ahead: int, scale: Optional[float] = None,
+                              out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """fp32 block-window attention (pa_block_window_attn_fwd_f32); q/k/v
+    [batch, n, H, D] float32."""
+    lib = load_library()
+    for t, nme in ((q, "q"), (k, "k"), (v, "v")):
+        _need(t, nme, torch.float32, 4)
+    if k.shape != q.shape or v.shape != q.shape:
+        raise ValueError("q, k, v must have the same [batch, n, H, D] shape")
+    batch, n, H, D = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    _need(out, "out", torch.float32, 4)
+    if out.shape != q.shape:
+        raise ValueError("out must have q's shape")
+    if scale is None:
+        scale = 1.0 / math.sqrt(D)
+    st = lib.pa_block_window_attn_fwd_f32(q.data_ptr(), k.data_ptr(), v.data_ptr(),
+                                          out.data_ptr(), batch, n, int(block), int(look_back),
+                                          int(look_ahead), H, D, float(scale), _stream(stream))
+    _check("pa_block_window_attn_fwd_f32", st)
     return out
 
 

@@ -31,7 +31,8 @@ def test_header_declares_expected_entry_points():
     for n in ["pa_varlen_attn_fwd", "pa_block_window_attn_fwd", "pa_cu_seqlens_from_lengths",
               "pa_pack", "pa_unpack", "pa_varlen_work_order", "pa_varlen_num_work_items",
               "pa_get_device_status", "pa_status_string", "pa_cfg_combine",
-              "pa_last_cuda_error", "pa_selftest_wait_timeout", "pa_rope_packed"]:
+              "pa_last_cuda_error", "pa_selftest_wait_timeout", "pa_rope_packed",
+              "pa_block_window_attn_fwd_f32"]:
         assert n in names
 
 
@@ -73,21 +74,23 @@ def test_varlen_host_checks(lib, kw, code):
     assert _varlen(lib, **kw) == code
 
 
-def _bw(lib, **kw):
+def _bw(lib, fn, **kw):
     args = dict(q=A, k=A, v=A, out=A, batch=1, n=2400, block=24, lb=0, la=0, H=16, D=64,
                 scale=0.125)
     args.update(kw)
-    return lib.pa_block_window_attn_fwd(args["q"], args["k"], args["v"], args["out"],
-                                        args["batch"], args["n"], args["block"], args["lb"],
-                                        args["la"], args["H"], args["D"], args["scale"], None)
+    return getattr(lib, fn)(args["q"], args["k"], args["v"], args["out"], args["batch"],
+                            args["n"], args["block"], args["lb"], args["la"], args["H"],
+                            args["D"], args["scale"], None)
 
 
+@pytest.mark.parametrize("fn", ["pa_block_window_attn_fwd", "pa_block_window_attn_fwd_f32"])
 @pytest.mark.parametrize("kw,code", [
     (dict(v=None), 1), (dict(n=0), 1), (dict(block=0), 1), (dict(lb=-1), 1), (dict(la=-1), 1),
-    (dict(scale=math.inf), 1), (dict(D=32), 2), (dict(k=MIS), 3),
+    (dict(scale=math.inf), 1), (dict(D=32), 2), (dict(k=MIS), 3), (dict(out=A + 4), 3),
+    (dict(batch=70000), 2), (dict(H=0), 1),
 ])
-def test_block_window_host_checks(lib, kw, code):
-    assert _bw(lib, **kw) == code
+def test_block_window_host_checks(lib, fn, kw, code):
+    assert _bw(lib, fn, **kw) == code
 
 
 def test_pack_and_scan_host_checks(lib):

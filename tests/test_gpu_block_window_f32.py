@@ -1,0 +1,111 @@
+"""Parity of the fp32 block-window attention with the fp64 dense
+block-difference mask oracle, through the C ABI.
+
+The bound is the one the pages saw between the fp32 block-local and the fp32
+dense masked attention of the Token2Wav DiT: 6e-6 ("[Perf][Model] Use
+block-sparse attention in Qwen2.5-Omni Token2Wav DiT", Test Result).  With
+unit-normal inputs an fp32 result carries a few 1e-7 of rounding (64-term dot
+products, exp, a 24-72-term weighted sum), so the max-abs bound is 6e-6 and
+the mean-abs bound 5e-7.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads
+
+pytestmark = pytest.mark.gpu
+
+MAX_ABS = 6e-6
+MEAN_ABS = 5e-7
+
+
+@pytest.fixture(scope="module")
+def pv():
+    import packed_varlen_gb300 as pv
+    pv.load_library()
+    pv.get_device_status()
+    return pv
+
+
+def _run(pv, w, lb, la):
+    q, k, v = w.q.cuda(), w.k.cuda(), w.v.cuda()
+    out = pv.block_window_attn_fwd_f32(q, k, v, w.block, lb, la, scale=w.scale)
+    torch.cuda.synchronize()
+    return out.cpu()
+
+
+def _close(got, want, what):
+    err = np.abs(oracle.to_f64(got) - want)
+    assert np.isfinite(oracle.to_f64(got)).all(), what
+    assert err.max() <= MAX_ABS, f"{what}: max abs {err.max():.3e}"
+    assert err.mean() <= MEAN_ABS, f"{what}: mean abs {err.mean():.3e}"
+
+
+LOOKS = [(0, 0), (1, 0), (0, 1), (1, 1), (2, 3)]
+
+
+@pytest.mark.parametrize("n", [1, 10, 24, 96, 101])
+@pytest.mark.parametrize("look", LOOKS)
+def test_pages_unit_cases(pv, n, look):
+    # one frame, shorter than a block, one block, whole blocks, a partial last block
+    w = workloads.random_block_window_f32(1, n, 4, 64, 24, seed=n + 10 * look[0] + look[1])
+    want = oracle.block_window_attention(w.q, w.k, w.v, 24, look[0], look[1], w.scale)
+    _close(_run(pv, w, *look), want, f"n={n} look={look}")
+
+
+@pytest.mark.parametrize("n", [2400, 2390])
+@pytest.mark.parametrize("look", [(0, 0), (1, 1)])
+def test_token2wav_cfg_batch(pv, n, look):
+    w = workloads.token2wav_f32(n=n)
+    want = oracle.block_window_attention(w.q, w.k, w.v, w.block, look[0], look[1], w.scale)
+    _close(_run(pv, w, *look), want, f"token2wav f32 n={n} look={look}")
+    assert pv.get_device_status() == 0
+
+
+@pytest.mark.parametrize("block,D", [(1, 64), (7, 128), (64, 64), (200, 128), (24, 128),
+                                     (13, 64)])
+def test_other_blocks_and_head_dims(pv, block, D):
+    w = workloads.random_block_window_f32(2, 333, 3, D, block, seed=block + D)
+    for lb, la in [(0, 0), (1, 2), (4, 0)]:
+        want = oracle.block_window_attention(w.q, w.k, w.v, block, lb, la, w.scale)
+        _close(_run(pv, w, lb, la), want, f"block={block} D={D} look=({lb},{la})")
+
+
+def test_window_covers_everything_is_dense(pv):
+    # look-back and look-ahead past both ends: plain dense attention
+    w = workloads.random_block_window_f32(1, 150, 2, 128, 24, seed=9)
+    for h in range(2):
+        dense = oracle.masked_attention(oracle.to_f64(w.q[0, :, h]), oracle.to_f64(w.k[0, :, h]),
+                                        oracle.to_f64(w.v[0, :, h]),
+                                        np.ones((150, 150), dtype=bool), w.scale)
+        got = _run(pv, w, 100, 100)[0, :, h]
+        err = np.abs(oracle.to_f64(got) - dense)
+        assert err.max() <= MAX_ABS
+
+
+def test_cfg_rows_match_single_batch_bitwise(pv):
+    # batch 2 (CFG) gives each entry exactly what a batch-1 call gives it
+    w = workloads.token2wav_f32(n=480)
+    both = _run(pv, w, 1, 1)
+    for b in range(2):
+        one = workloads.BlockWindowWorkload("one", 1, 480, 16, 64, 24, [(1, 1)],
+                                            w.q[b:b + 1].clone(), w.k[b:b + 1].clone(),
+                                            w.v[b:b + 1].clone(), 0)
+        assert torch.equal(both[b:b + 1].view(torch.int32), _run(pv, one, 1, 1).view(torch.int32))
+
+
+def test_repeatable_with_guard_band(pv):
+    w = workloads.random_block_window_f32(2, 257, 4, 64, 24, seed=11)
+    a = _run(pv, w, 1, 1)
+    b = _run(pv, w, 1, 1)
+    assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+    # rows outside out's extent are never written: a guard band stays intact
+    q, k, v = w.q.cuda(), w.k.cuda(), w.v.cuda()
+    buf = torch.full((2 * 257 * 4 * 64 + 64,), 7.0, device="cuda")
+    out = buf[:2 * 257 * 4 * 64].view(2, 257, 4, 64)
+    pv.block_window_attn_fwd_f32(q, k, v, 24, 1, 1, scale=w.scale, out=out)
+    torch.cuda.synchronize()
+    assert (buf[2 * 257 * 4 * 64:] == 7.0).all()
+    assert torch.equal(out.cpu().view(torch.int32), a.view(torch.int32))

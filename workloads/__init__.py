@@ -202,6 +202,28 @@ def token2wav(n: int = 2400, seed: int = 4) -> BlockWindowWorkload:
                                list(TOKEN2WAV_LAYERS), q, k, v, seed)
 
 
+def token2wav_f32(n: int = 2400, seed: int = 6) -> BlockWindowWorkload:
+    """The Token2Wav DiT's attention in its own dtype: fp32, classifier-free
+    guidance as batch 2 (conditional and unconditional rows), H=16, D=64,
+    block 24, the same 22 layers."""
+    g = torch.Generator().manual_seed(seed)
+    shape = (2, n, 16, 64)
+    q = torch.randn(*shape, generator=g, dtype=torch.float32)
+    k = torch.randn(*shape, generator=g, dtype=torch.float32)
+    v = torch.randn(*shape, generator=g, dtype=torch.float32)
+    return BlockWindowWorkload("token2wav_block_window_f32", 2, n, 16, 64, 24,
+                               list(TOKEN2WAV_LAYERS), q, k, v, seed)
+
+
+def random_block_window_f32(batch: int, n: int, H: int, D: int, block: int, seed: int,
+                            layers=None) -> BlockWindowWorkload:
+    g = torch.Generator().manual_seed(seed)
+    shape = (batch, n, H, D)
+    q, k, v = (torch.randn(*shape, generator=g, dtype=torch.float32) for _ in range(3))
+    return BlockWindowWorkload(f"block_window_f32_n{n}", batch, n, H, D, block,
+                               list(layers or [(0, 0)]), q, k, v, seed)
+
+
 def padded(lengths: List[int], H: int, D: int, seed: int,
            s_max: Optional[int] = None, name: str = "padded") -> PaddedWorkload:
     """Padded [B, S_max, H, D] q/k/v for the given lengths (every row drawn,
