@@ -4,16 +4,32 @@
 // dense masked SDPA to 6e-6, Test Result).  Query i of a batch entry sees
 // key j iff j < n and -look_back <= block(j) - block(i) <= look_ahead.
 //
-// All arithmetic is IEEE fp32 on the CUDA cores (the tensor cores' tf32 path
-// keeps 10 mantissa bits, far from the 6e-6 the fp32 model needs).  The
-// layer is small and latency bound.  A CTA owns 32 query rows of one head,
-// 8 per warp, and walks the union of their key windows in 32-key chunks
-// staged in shared memory.  Scores: a lane per key; each lane keeps a float4
-// of its K row in registers and multiplies it against the 8 rows' Q (shared
-// memory broadcasts), so one K load feeds 8 rows.  The running max is
-// warp-wide; the running sum stays lane-partial until the end.  P V: the
-// warp's P goes through shared memory as float4 broadcasts and each lane
-// owns D/32 output dimensions of all 8 rows.
+// All arithmetic is fp32 on the CUDA cores, packed two lanes wide (fma.rn
+// on float2: each component rounds exactly like fmaf); the tensor cores' tf32
+// path keeps 10 mantissa bits, far from the 6e-6 the fp32 model needs.  The
+// softmax runs in base 2: q is scaled once by scale * log2(e), so a score is
+// already a power of two and the exponentials are the hardware ex2.
+//
+// Work split.  Rows of one block share one key window, so a warp task is a
+// run of at most kRows rows inside one block.  kSplit = 2 lanes share a
+// group of kRL rows and each owns D / 2 of their dimensions (float4 slots i
+// with i % 2 == its part): D = 64 takes two rows per lane pair (kRL = 2,
+// 32 rows a task), D = 128 one (kRL = 1, 16 rows a task).  A lane keeps
+// its q slices and output accumulators in registers.  The window's keys are
+// the same for the whole warp, so every K or V load is a broadcast of two
+// adjacent 16-byte words; such a 128-bit load costs two shared-memory
+// wavefronts (512 bytes reach the warp's registers), and with kRL = 2 each
+// loaded float feeds two FMAs, which keeps shared memory at the FP32 pipes'
+// rate.  The online softmax runs per lane and row; one shuffle finishes a
+// score.
+//
+// Pipeline.  Every warp is its own pipeline: it owns a run of consecutive
+// tasks and streams, for each, the task's q rows and then its window in
+// kStage-key K/V stages through a private kBuf-slot shared-memory ring filled
+// by cp.async, so the next stages (and the next task's q) arrive while the
+// current one computes.  Warps never wait for one another.  q is stored with
+// its 16-byte chunks XOR-swizzled by row, so the lanes' reads of their own
+// rows hit distinct banks.
 #include <math.h>
 #include <stdint.h>
 
@@ -22,185 +38,310 @@
 namespace pa {
 namespace {
 
-constexpr int kRows = 32;                 // query rows per CTA
 constexpr int kWarps = 4;
-constexpr int kRpw = kRows / kWarps;      // rows per warp
-constexpr int kChunk = 32;                // keys per staged chunk (a lane per key)
 constexpr int kThreads = kWarps * 32;
-
-template <int D>
-struct F32Smem {
-  static constexpr int kKs = D + 4;       // padded K row: float4 reads hit 32 banks
-  static constexpr int kQ = 0;                              // [kRows][D]
-  static constexpr int kK = kQ + kRows * D;                 // [kChunk][kKs]
-  static constexpr int kV = kK + kChunk * kKs;              // [kChunk][D]
-  static constexpr int kP = kV + kChunk * D;                // [kWarps][kRpw][kChunk]
-  static constexpr int kFloats = kP + kWarps * kRpw * kChunk;
-  static constexpr int kBytes = kFloats * 4;
-};
+constexpr int kStage = 16;    // keys per K/V stage (a multiple of kGroup)
+constexpr int kBuf = 3;       // ring slots per warp
 
 struct BwF32Params {
   const float *q, *k, *v;
   float *out;
-  int64_t row_stride;  // H * D
-  float scale;
+  int64_t row_stride;   // H * D
+  float q_scale;        // scale * log2(e)
   int n, block, look_back, look_ahead;
+  int H;
+  int64_t tasks_per_row;   // tasks of one (batch entry, head)
+  int64_t n_tasks;         // over all batch entries and heads
+  int tasks_per_warp;
 };
 
-// [lo, hi): the keys query i may attend to.
-__device__ __forceinline__ void window(const BwF32Params &p, int i, int &lo, int &hi) {
-  const int64_t b = i / p.block;
+// One warp task: rows [row_lo, row_hi) of one (batch entry, head) and their
+// key window [lo, hi); `off` is the element offset of (entry, row 0, head).
+struct Task {
+  int64_t off;
+  int row_lo, row_hi, lo, hi;
+};
+
+template <int kRows, int D>
+__device__ __forceinline__ Task task_of(const BwF32Params &p, int64_t T) {
+  const int segs = (p.block + kRows - 1) / kRows;
+  const int64_t rid = T / p.tasks_per_row;          // (batch entry, head)
+  const int64_t t = T - rid * p.tasks_per_row;
+  const int64_t seq = rid / p.H, h = rid - seq * p.H;
+  const int64_t b = t / segs;
+  const int64_t first = b * p.block + (t - b * segs) * kRows;
+  int64_t last = first + kRows;
+  if (last > (b + 1) * p.block) last = (b + 1) * p.block;
+  if (last > p.n) last = p.n;
   const int64_t l = (b - p.look_back) * p.block;
-  const int64_t h = (b + 1 + p.look_ahead) * p.block;
-  lo = static_cast<int>(l > 0 ? l : 0);
-  hi = static_cast<int>(h < p.n ? h : p.n);
+  const int64_t hh = (b + 1 + p.look_ahead) * p.block;
+  Task k;
+  k.off = seq * p.n * p.row_stride + h * D;
+  k.row_lo = static_cast<int>(first);
+  k.row_hi = static_cast<int>(last);
+  k.lo = static_cast<int>(l > 0 ? l : 0);
+  k.hi = static_cast<int>(hh < p.n ? hh : p.n);
+  return k;
+}
+
+__device__ __forceinline__ int kv_stages(const Task &k) {
+  return (k.hi - k.lo + kStage - 1) / kStage;
+}
+
+__device__ __forceinline__ void cp_async16(float *smem_dst, const float *src, bool valid) {
+  const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
+               "r"(valid ? 16 : 0)
+               : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;\n" ::: "memory");
+}
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
+}
+__device__ __forceinline__ float exp2_hw(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
+  return y;
 }
 
 template <int D>
+struct F32Shape {
+  static constexpr int kSplit = 2;                  // lanes per row group
+  static constexpr int kRL = D == 64 ? 2 : 1;       // rows per lane
+  static constexpr int kRows = 32 / kSplit * kRL;   // rows per warp task
+  static constexpr int kGroup = 8 / kRL;            // keys per online-softmax update
+};
+
+template <int D>
 __global__ void __launch_bounds__(kThreads) block_window_f32_kernel(const BwF32Params p) {
-  using L = F32Smem<D>;
+  using S = F32Shape<D>;
+  constexpr int kSplit = S::kSplit, kRL = S::kRL, kRows = S::kRows, kGroup = S::kGroup;
+  constexpr int kD4 = D / 4;                  // float4 per row
+  constexpr int kF4 = kD4 / kSplit;           // float4 slots per lane and row
+  constexpr int kSlot = 2 * kStage * D;       // floats per ring slot: K and V of a stage
+  static_assert(kRows * D <= kSlot, "a slot holds a task's q rows");
+  static_assert(kStage % kGroup == 0, "stages hold whole groups");
+  constexpr int kSwzP = 8 / kSplit;           // row groups per swizzle period
   extern __shared__ __align__(16) float smem[];
-  float *sQ = smem + L::kQ;
-  float *sK = smem + L::kK;
-  float *sV = smem + L::kV;
-  constexpr int kPerLane = D / 32;
-  constexpr int kD4 = D / 4;
 
-  const int h = blockIdx.y, seq = blockIdx.z;
-  const int r0 = blockIdx.x * kRows;
-  const int n_rows = min(kRows, p.n - r0);
-  const int64_t base = static_cast<int64_t>(seq) * p.n;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  float *sP = smem + L::kP + warp * kRpw * kChunk;
+  float *ring = smem + warp * kBuf * kSlot;
+  const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+  const int64_t t_begin = gw * p.tasks_per_warp;
+  int64_t t_end = t_begin + p.tasks_per_warp;
+  if (t_end > p.n_tasks) t_end = p.n_tasks;
+  if (t_begin >= t_end) return;   // warps share nothing: an idle warp may leave
 
-  for (int idx = threadIdx.x; idx < kRows * kD4; idx += kThreads) {
-    const int r = idx / kD4, d4 = idx % kD4;
-    float4 x = make_float4(0.f, 0.f, 0.f, 0.f);
-    if (r < n_rows)
-      x = *reinterpret_cast<const float4 *>(p.q + (base + r0 + r) * p.row_stride + h * D + 4 * d4);
-    *reinterpret_cast<float4 *>(sQ + r * D + 4 * d4) = x;
-  }
-  int k_lo, k_hi, unused;
-  window(p, r0, k_lo, unused);
-  window(p, r0 + n_rows - 1, unused, k_hi);
+  // q chunk c of task row r sits at chunk c ^ swz(r): the lanes reading one
+  // chunk of their rows hit distinct banks
+  auto swz = [](int r) { return ((r / kRL) % kSwzP) * kSplit; };
 
-  float m[kRpw], l[kRpw], acc[kRpw][kPerLane];
-  int lo[kRpw], hi[kRpw];
-  int w_lo = p.n, w_hi = 0;   // union of the warp's live rows' windows
+  // ---- producer cursor: stage `is` of task `it` (0: q rows, 1..: K/V) ----
+  int64_t it = t_begin;
+  int is = 0;
+  Task ti = task_of<kRows, D>(p, it);
+  int slot_in = 0;
+  auto issue_next = [&]() {
+    if (it < t_end) {
+      float *dst = ring + slot_in * kSlot;
+      if (is == 0) {
+        for (int idx = lane; idx < kRows * kD4; idx += 32) {
+          const int r = idx / kD4, c = idx % kD4;
+          const bool ok = ti.row_lo + r < ti.row_hi;
+          cp_async16(dst + r * D + 4 * (c ^ swz(r)),
+                     p.q + (ok ? ti.off + (ti.row_lo + r) * p.row_stride + 4 * c : 0), ok);
+        }
+      } else {
+        const int kt = ti.lo + (is - 1) * kStage;
+        for (int idx = lane; idx < kStage * kD4; idx += 32) {
+          const int j = idx / kD4, c = idx % kD4;
+          const bool ok = kt + j < ti.hi;
+          const int64_t src = ok ? ti.off + (kt + j) * p.row_stride + 4 * c : 0;
+          cp_async16(dst + j * D + 4 * c, p.k + src, ok);
+          cp_async16(dst + kStage * D + j * D + 4 * c, p.v + src, ok);
+        }
+      }
+      if (++is > kv_stages(ti)) {
+        is = 0;
+        if (++it < t_end) ti = task_of<kRows, D>(p, it);
+      }
+    }
+    cp_async_commit();   // an empty group past the end keeps the count uniform
+    slot_in = slot_in + 1 == kBuf ? 0 : slot_in + 1;
+  };
 #pragma unroll
-  for (int rr = 0; rr < kRpw; ++rr) {
-    m[rr] = -INFINITY;
-    l[rr] = 0.f;
+  for (int s = 0; s < kBuf - 1; ++s) issue_next();
+
+  // ---- consumer ----
+  const int part = lane % kSplit;
+  const int r0 = (lane / kSplit) * kRL;   // this lane's first task row
+  float2 q2[kRL][2 * kF4], acc2[kRL][2 * kF4];
+  float m[kRL], l[kRL];
+  Task tc{0, 0, 0, 0, 0};
+  int cs = 0, n_kv = 0, slot = 0;
+  for (int64_t ct = t_begin; ct < t_end;) {
+    cp_async_wait<kBuf - 2>();
+    __syncwarp();          // the slot's copies from every lane are visible
+    issue_next();          // refills the slot consumed last round
+    const float *cur = ring + slot * kSlot;
+    if (cs == 0) {
+      tc = task_of<kRows, D>(p, ct);
+      n_kv = kv_stages(tc);
+      const float2 s2 = make_float2(p.q_scale, p.q_scale);
 #pragma unroll
-    for (int e = 0; e < kPerLane; ++e) acc[rr][e] = 0.f;
-    const int r = warp * kRpw + rr;
-    if (r < n_rows) {
-      window(p, r0 + r, lo[rr], hi[rr]);
-      w_lo = min(w_lo, lo[rr]);
-      w_hi = max(w_hi, hi[rr]);
+      for (int rr = 0; rr < kRL; ++rr) {
+        const float4 *qr = reinterpret_cast<const float4 *>(cur + (r0 + rr) * D);
+#pragma unroll
+        for (int i = 0; i < kF4; ++i) {
+          const float4 x = qr[(i * kSplit + part) ^ swz(r0 + rr)];
+          q2[rr][2 * i] = __fmul2_rn(make_float2(x.x, x.y), s2);
+          q2[rr][2 * i + 1] = __fmul2_rn(make_float2(x.z, x.w), s2);
+        }
+#pragma unroll
+        for (int i = 0; i < 2 * kF4; ++i) acc2[rr][i] = make_float2(0.f, 0.f);
+        m[rr] = -INFINITY;
+        l[rr] = 0.f;
+      }
     } else {
-      lo[rr] = hi[rr] = 0;   // a row past n sees no key
-    }
-  }
-
-  for (int kt = k_lo; kt < k_hi; kt += kChunk) {
-    __syncthreads();  // previous chunk consumed; sQ written, first time
-    for (int idx = threadIdx.x; idx < kChunk * kD4; idx += kThreads) {
-      const int j = idx / kD4, d4 = idx % kD4;
-      float4 kk = make_float4(0.f, 0.f, 0.f, 0.f), vv = kk;
-      if (kt + j < k_hi) {
-        const int64_t off = (base + kt + j) * p.row_stride + h * D + 4 * d4;
-        kk = *reinterpret_cast<const float4 *>(p.k + off);
-        vv = *reinterpret_cast<const float4 *>(p.v + off);
-      }
-      *reinterpret_cast<float4 *>(sK + j * L::kKs + 4 * d4) = kk;
-      *reinterpret_cast<float4 *>(sV + j * D + 4 * d4) = vv;
-    }
-    __syncthreads();
-    if (w_hi <= kt || kt + kChunk <= w_lo) continue;   // warp-uniform
-
-    float s[kRpw];
+      const int kt = tc.lo + (cs - 1) * kStage;
+      const int e = tc.hi < kt + kStage ? tc.hi : kt + kStage;
+      const float4 *k4 = reinterpret_cast<const float4 *>(cur) + part;
+      const float4 *v4 = reinterpret_cast<const float4 *>(cur + kStage * D) + part;
 #pragma unroll
-    for (int rr = 0; rr < kRpw; ++rr) s[rr] = 0.f;
-    const float4 *krow = reinterpret_cast<const float4 *>(sK + lane * L::kKs);
-    const float4 *qw = reinterpret_cast<const float4 *>(sQ + warp * kRpw * D);
-#pragma unroll 4
-    for (int d4 = 0; d4 < kD4; ++d4) {
-      const float4 kk = krow[d4];
+      for (int g0 = 0; g0 < kStage; g0 += kGroup) {
+        const int g = kt + g0;
+        if (g >= e) break;   // warp-uniform
+        float2 sc2[kRL][kGroup];
 #pragma unroll
-      for (int rr = 0; rr < kRpw; ++rr) {
-        const float4 qq = qw[rr * kD4 + d4];
-        s[rr] = fmaf(qq.x, kk.x, s[rr]);
-        s[rr] = fmaf(qq.y, kk.y, s[rr]);
-        s[rr] = fmaf(qq.z, kk.z, s[rr]);
-        s[rr] = fmaf(qq.w, kk.w, s[rr]);
-      }
-    }
-    const int key = kt + lane;
+        for (int rr = 0; rr < kRL; ++rr)
 #pragma unroll
-    for (int rr = 0; rr < kRpw; ++rr) {
-      const bool ok = key >= lo[rr] && key < hi[rr];
-      const float x = ok ? s[rr] * p.scale : -INFINITY;
-      float cmax = x;
+          for (int kk = 0; kk < kGroup; ++kk) sc2[rr][kk] = make_float2(0.f, 0.f);
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) cmax = fmaxf(cmax, __shfl_xor_sync(0xffffffffu, cmax, o));
-      const float m_new = fmaxf(m[rr], cmax);
-      // no key of this row in the chunk: nothing changes
-      const float alpha = m_new == -INFINITY ? 1.f : expf(m[rr] - m_new);
-      const float pj = ok ? expf(x - m_new) : 0.f;
-      l[rr] = l[rr] * alpha + pj;
-      m[rr] = m_new;
+        for (int i = 0; i < kF4; ++i) {
 #pragma unroll
-      for (int e = 0; e < kPerLane; ++e) acc[rr][e] *= alpha;
-      sP[rr * kChunk + lane] = pj;
-    }
-    __syncwarp();
-#pragma unroll 2
-    for (int j4 = 0; j4 < kChunk / 4; ++j4) {
-      float4 pp[kRpw];
+          for (int kk = 0; kk < kGroup; ++kk) {
+            const float4 kv = k4[(g0 + kk) * kD4 + i * kSplit];
 #pragma unroll
-      for (int rr = 0; rr < kRpw; ++rr)
-        pp[rr] = *reinterpret_cast<const float4 *>(sP + rr * kChunk + 4 * j4);
+            for (int rr = 0; rr < kRL; ++rr) {
+              sc2[rr][kk] = __ffma2_rn(q2[rr][2 * i], make_float2(kv.x, kv.y), sc2[rr][kk]);
+              sc2[rr][kk] = __ffma2_rn(q2[rr][2 * i + 1], make_float2(kv.z, kv.w), sc2[rr][kk]);
+            }
+          }
+        }
+        float pr[kRL][kGroup], alpha[kRL];
 #pragma unroll
-      for (int jj = 0; jj < 4; ++jj) {
-        const float *vrow = sV + (4 * j4 + jj) * D + lane;
+        for (int rr = 0; rr < kRL; ++rr) {
 #pragma unroll
-        for (int e = 0; e < kPerLane; ++e) {
-          const float ve = vrow[32 * e];
+          for (int kk = 0; kk < kGroup; ++kk) {
+            float x = sc2[rr][kk].x + sc2[rr][kk].y;
+            x += __shfl_xor_sync(0xffffffffu, x, 1);
+            pr[rr][kk] = g + kk < e ? x : -INFINITY;   // keys past e: zero-filled rows
+          }
+          float mx = pr[rr][0];
 #pragma unroll
-          for (int rr = 0; rr < kRpw; ++rr) {
-            const float pb = jj == 0 ? pp[rr].x : jj == 1 ? pp[rr].y : jj == 2 ? pp[rr].z : pp[rr].w;
-            acc[rr][e] = fmaf(pb, ve, acc[rr][e]);
+          for (int kk = 1; kk < kGroup; ++kk) mx = fmaxf(mx, pr[rr][kk]);
+          const float m_new = fmaxf(m[rr], mx);       // finite: key g is in the window
+          alpha[rr] = exp2_hw(m[rr] - m_new);         // 0 on the first group
+          m[rr] = m_new;
+          float psum = 0.f;
+#pragma unroll
+          for (int kk = 0; kk < kGroup; ++kk) {
+            pr[rr][kk] = exp2_hw(pr[rr][kk] - m_new);
+            psum += pr[rr][kk];
+          }
+          l[rr] = l[rr] * alpha[rr] + psum;
+        }
+#pragma unroll
+        for (int i = 0; i < kF4; ++i) {
+          float2 lo2[kRL], hi2[kRL];
+#pragma unroll
+          for (int rr = 0; rr < kRL; ++rr) {
+            const float2 al2 = make_float2(alpha[rr], alpha[rr]);
+            lo2[rr] = __fmul2_rn(acc2[rr][2 * i], al2);
+            hi2[rr] = __fmul2_rn(acc2[rr][2 * i + 1], al2);
+          }
+#pragma unroll
+          for (int kk = 0; kk < kGroup; ++kk) {
+            const float4 vv = v4[(g0 + kk) * kD4 + i * kSplit];
+#pragma unroll
+            for (int rr = 0; rr < kRL; ++rr) {
+              const float2 pk = make_float2(pr[rr][kk], pr[rr][kk]);
+              lo2[rr] = __ffma2_rn(pk, make_float2(vv.x, vv.y), lo2[rr]);
+              hi2[rr] = __ffma2_rn(pk, make_float2(vv.z, vv.w), hi2[rr]);
+            }
+          }
+#pragma unroll
+          for (int rr = 0; rr < kRL; ++rr) {
+            acc2[rr][2 * i] = lo2[rr];
+            acc2[rr][2 * i + 1] = hi2[rr];
           }
         }
       }
     }
-    __syncwarp();  // sP is rewritten by the next chunk
+    __syncwarp();   // every lane is done with this slot before it is refilled
+    slot = slot + 1 == kBuf ? 0 : slot + 1;
+    if (cs == n_kv) {
+#pragma unroll
+      for (int rr = 0; rr < kRL; ++rr) {
+        const int row = tc.row_lo + r0 + rr;
+        if (row < tc.row_hi) {
+          // both parts of a row hold the same l: each saw every score
+          const float inv = 1.f / l[rr];   // l > 0: a row always sees its own block
+          float4 *dst = reinterpret_cast<float4 *>(p.out + tc.off + row * p.row_stride);
+#pragma unroll
+          for (int i = 0; i < kF4; ++i)
+            dst[i * kSplit + part] =
+                make_float4(acc2[rr][2 * i].x * inv, acc2[rr][2 * i].y * inv,
+                            acc2[rr][2 * i + 1].x * inv, acc2[rr][2 * i + 1].y * inv);
+        }
+      }
+      cs = 0;
+      ++ct;
+    } else {
+      ++cs;
+    }
   }
-#pragma unroll
-  for (int rr = 0; rr < kRpw; ++rr) {
-    float sum = l[rr];
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, o);
-    const int r = warp * kRpw + rr;
-    if (r >= n_rows) continue;
-    const float inv = sum > 0.f ? 1.f / sum : 0.f;
-    float *dst = p.out + (base + r0 + r) * p.row_stride + h * D + lane;
-#pragma unroll
-    for (int e = 0; e < kPerLane; ++e) dst[32 * e] = acc[rr][e] * inv;
-  }
+  cp_async_wait<0>();   // nothing in flight at exit
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 template <int D>
-cudaError_t launch_f32(const BwF32Params &p, int batch, int H, cudaStream_t st) {
+cudaError_t launch_f32(BwF32Params p, int batch, int H, cudaStream_t st) {
+  constexpr int kRows = F32Shape<D>::kRows;
+  constexpr int kSmem = kWarps * kBuf * 2 * kStage * D * 4;
   static unsigned long long done = 0;
   cudaError_t e = set_smem_once(reinterpret_cast<const void *>(&block_window_f32_kernel<D>),
-                                F32Smem<D>::kBytes, done);
+                                kSmem, done);
   if (e != cudaSuccess) return e;
-  dim3 grid((p.n + kRows - 1) / kRows, H, batch);
-  block_window_f32_kernel<D><<<grid, kThreads, F32Smem<D>::kBytes, st>>>(p);
+  // resident CTAs per SM, per device (a benign race: every writer stores the same value)
+  static int resident[64];
+  int dev = 0, sms = 0;
+  if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
+  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
+    return e;
+  int per_sm = resident[dev & 63];
+  if (per_sm == 0) {
+    if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, block_window_f32_kernel<D>,
+                                                           kThreads, kSmem)) != cudaSuccess)
+      return e;
+    if (per_sm < 1) per_sm = 1;
+    __atomic_store_n(&resident[dev & 63], per_sm, __ATOMIC_RELAXED);
+  }
+  const int64_t segs = (p.block + kRows - 1) / kRows;
+  p.H = H;
+  p.tasks_per_row = ((static_cast<int64_t>(p.n) + p.block - 1) / p.block) * segs;
+  p.n_tasks = p.tasks_per_row * H * batch;
+  // every warp resident at once: each takes an equal run of tasks
+  const int64_t warps = static_cast<int64_t>(sms) * per_sm * kWarps;
+  const int64_t tpw = (p.n_tasks + warps - 1) / warps;
+  if (tpw > 0x7fffffff) return cudaErrorInvalidConfiguration;
+  p.tasks_per_warp = static_cast<int>(tpw);
+  const int64_t ctas = (p.n_tasks + tpw * kWarps - 1) / (tpw * kWarps);
+  block_window_f32_kernel<D><<<static_cast<unsigned>(ctas), kThreads, kSmem, st>>>(p);
   return cudaGetLastError();
 }
 
@@ -220,8 +361,10 @@ extern "C" pa_status pa_block_window_attn_fwd_f32(const float *q, const float *k
   if ((D != 64 && D != 128) || H > 65535 || batch > 65535) return PA_ERR_UNSUPPORTED;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
     return PA_ERR_MISALIGNED;
-  BwF32Params p{q, k, v, out, static_cast<int64_t>(H) * D, scale, n, block, look_back,
-                look_ahead};
+  const float q_scale = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
+  if (!isfinite(q_scale)) return PA_ERR_INVALID_ARG;
+  BwF32Params p{q, k, v, out, static_cast<int64_t>(H) * D, q_scale, n, block, look_back,
+                look_ahead, H, 0, 0, 0};
   auto st = reinterpret_cast<cudaStream_t>(stream);
   return from_cuda(D == 64 ? launch_f32<64>(p, batch, H, st) : launch_f32<128>(p, batch, H, st));
 }
