@@ -24,14 +24,18 @@ the integer steps), written for a reader to check against the definitions:
 * ``cfg_combine``: segment-aware unpack of each request's image span with the
   per-request classifier-free-guidance combine ("feat: Support dynamic
   batching for heterogeneous diffusion requests", CFG behavior).
+* ``linear``: the packed-M projection y = x w^T + bias ("feat: Support
+  dynamic batching ...", packed varlen step batching, Determinism).
 
 Every function is pinned by tests in ``tests/test_oracle_pins.py`` and
-``tests/test_oracle_cfg.py`` and ``tests/test_oracle_rope.py`` against
+``tests/test_oracle_cfg.py``, ``tests/test_oracle_rope.py`` and
+``tests/test_oracle_linear.py`` against
 brute force, closed forms, a library routine and the pages' invariants.
 """
 from .packing import cu_seqlens_from_lengths, pack, unpack, work_order
 from .cfg import cfg_combine
 from .rope import rope, rope_positions
+from .linear import linear, linear_rows, linear_flops
 from .attention import (
     masked_attention,
     varlen_mask,
@@ -49,4 +53,5 @@ __all__ = [
     "masked_attention", "varlen_mask", "varlen_attention", "key_padding_attention",
     "block_window_mask", "block_window_attention", "to_f64",
     "varlen_useful_flops", "block_window_useful_flops", "cfg_combine", "rope", "rope_positions",
+    "linear", "linear_rows", "linear_flops",
 ]
