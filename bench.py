@@ -85,7 +85,7 @@ def _kernel_digest() -> str:
     to the code it was taken on)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "packed_varlen_gb300", "csrc")
-    for name in ("attn_tc.cu", "tc_ptx.cuh", "sched.cuh", "internal.h"):
+    for name in ("attn_tc.cu", "tc_ptx.cuh", "sched.cuh", "internal.h", "tma_map.h"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())
@@ -347,6 +347,7 @@ def run_ours(args):
         raise RuntimeError("device status error during the timed run")
     cfg_meas = measure_cfg_combine(dev, 3072, 10, 3)
     rope_meas = measure_rope(dev, 10, 3)
+    linear_meas = measure_linear(dev, 10, 3)
 
     peaks, peak_src = _peaks()
     attn_mean_ms = statistics.mean(attn_ms)
@@ -396,6 +397,7 @@ def run_ours(args):
                                      / peaks["hbm_gbs"]),
             "cfg_combine": cfg_meas,
             "rope": rope_meas,
+            "linear": linear_meas,
         }
         print(json.dumps(result), flush=True)
     if dist:
@@ -416,6 +418,8 @@ def run_attn_only(args):
         return run_block_window_only(args, dev)
     if args.workload.startswith("cfg_combine"):
         return run_cfg_combine_only(args, dev)
+    if args.workload in ("linear_qkv", "linear_out"):
+        return run_linear_only(args, dev)
     if args.workload == "rope":
         print(json.dumps(measure_rope(dev, args.steps, args.warmup)), flush=True)
         return 0
@@ -595,6 +599,57 @@ def measure_rope(dev, steps, warmup):
             "peak_source": src}
 
 
+def measure_linear(dev, steps, warmup, kinds=("qkv", "out")):
+    """The batch-invariant packed-M projections of the mixed-resolution batch
+    (x [T, 3072] times the fused QKV or the output weight, with bias), each
+    launch after an L2 flush.  cuBLAS (torch's linear, not batch invariant)
+    is timed on the same operands for context."""
+    import packed_varlen_gb300 as pv
+    peaks, src = _peaks()
+    flusher = L2Flusher(dev)
+    stream = torch.cuda.current_stream()
+    res = {}
+    for kind in kinds:
+        w = workloads.mmdit_projection(kind)
+        x, wt, b = w.x.to(dev), w.w.to(dev), w.bias.to(dev)
+        y = torch.empty(w.M, w.N, dtype=torch.bfloat16, device=dev)
+        flops = 2 * w.M * w.N * w.K
+
+        def timed(fn):
+            for _ in range(warmup):
+                fn()
+            ts = []
+            for _ in range(steps):
+                flusher.flush()
+                e0 = torch.cuda.Event(enable_timing=True)
+                e1 = torch.cuda.Event(enable_timing=True)
+                e0.record(stream)
+                fn()
+                e1.record(stream)
+                ts.append((e0, e1))
+            torch.cuda.synchronize()
+            return statistics.median(a.elapsed_time(c) for a, c in ts)
+
+        ms = timed(lambda: pv.linear_bf16(x, wt, b, out=y))
+        ms_cublas = timed(lambda: torch.nn.functional.linear(x, wt, b))
+        if pv.get_device_status() != 0:
+            raise RuntimeError("device status error")
+        tf = flops / (ms * 1e-3) / 1e12
+        res[kind] = {"workload": f"{w.name}: M={w.M} (requests {w.lengths}), N={w.N}, K={w.K}",
+                     "flops": flops, "us": 1e3 * ms, "tflops": tf,
+                     "frac": tf / peaks["bf16_tflops"], "peak_source": f"{src} bf16 dense (burst)",
+                     "cublas_us": 1e3 * ms_cublas,
+                     "cublas_tflops": flops / (ms_cublas * 1e-3) / 1e12}
+    return res
+
+
+def run_linear_only(args, dev):
+    kind = args.workload.split("_", 1)[1]
+    print(json.dumps(dict(measure_linear(dev, args.steps, args.warmup, kinds=(kind,)),
+                          workload_name=args.workload)), flush=True)
+    return 0
+
+
 def measure_block_window(pv, bw, f32, dev, flusher, stream, reps=20):
     """Median time of each Token2Wav layer type with a clean L2 before every
     launch; bytes = q, k, v read once and out written once."""
@@ -690,6 +745,7 @@ def main():
                     help="time the attention kernel alone (profiling); not the bench line")
     ap.add_argument("--workload", default="single_8k",
                     help="with --attn-only: a varlen config name, single_<N>k, token2wav, token2wav_f32, "
+                         "linear_qkv, linear_out, "
                          "cfg_combine, cfg_combine_3072 or rope")
     args = ap.parse_args()
     if args.attn_only:

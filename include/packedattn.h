@@ -124,8 +124,9 @@ pa_status pa_block_window_attn_fwd(const void *q, const void *k, const void *v, 
  * SDPA (Test Result).  The window rule and the argument rules are those of
  * pa_block_window_attn_fwd; q, k, v, out are fp32 [batch, n, H, D]
  * contiguous, 16-byte aligned, caller-owned; out must not overlap q, k or v.
- * Every product and sum is IEEE fp32 (no tensor-core tf32), exponentials by
- * expf, so the result is within a few fp32 roundings of the exact one.
+ * Every product and sum is IEEE fp32 (no tensor-core tf32); the softmax runs
+ * in base 2 on the hardware exp2 with scale * log2(e) folded into q, so the
+ * result is within a few fp32 roundings of the exact one.
  */
 pa_status pa_block_window_attn_fwd_f32(const float *q, const float *k, const float *v,
                                        float *out, int32_t batch, int32_t n, int32_t block,
@@ -196,6 +197,30 @@ pa_status pa_rope_packed(void *q, void *k, const int32_t *cu_seqlens_q,
                          const int32_t *cu_seqlens_k, const int32_t *pos_offset,
                          int32_t batch, int32_t total_q, int32_t total_k, int32_t H,
                          int32_t D, float base, pa_stream_t stream);
+
+/*
+ * pa_linear_bf16 -- batch-invariant packed-M linear layer.
+ *
+ *   y[m, n] = sum_k x[m, k] * w[n, k] + bias[n]
+ *
+ * The packed path runs its projections on the flat [total_tokens, C]
+ * activations of all requests at once, and batched and serial outputs are
+ * bit-identical because these GEMMs give each row the same result whatever
+ * the packed M is ("feat: Support dynamic batching for heterogeneous
+ * diffusion requests", packed varlen step batching: Setup, Determinism;
+ * Notes, item 1).  Here every M runs one tile shape with a fixed K order and
+ * no split-K, so row m of y depends only on row m of x, w and bias: rows
+ * computed packed, alone or at any row offset are equal bit for bit.
+ *
+ * x [M, K], w [N, K] (out_features x in_features), y [M, N]: bf16 row-major
+ * contiguous, device, caller-owned; bias: bf16 [N] or NULL.  Accumulation
+ * in fp32, bias added in fp32, one round to bf16 (nearest even).  M >= 0
+ * (M = 0 does nothing and x, y may then be NULL), N >= 1, K >= 1; K and N
+ * multiples of 8 and every pointer 16-byte aligned, else PA_ERR_MISALIGNED.
+ * y must not overlap x, w or bias.
+ */
+pa_status pa_linear_bf16(const void *x, const void *w, const void *bias, void *y, int32_t M,
+                         int32_t N, int32_t K, pa_stream_t stream);
 
 /*
  * pa_cfg_combine -- segment-aware unpack of each request's image span with

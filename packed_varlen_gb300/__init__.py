@@ -60,6 +60,7 @@ _SIGNATURES = {
     "pa_last_cuda_error": ([], ctypes.c_char_p),
     "pa_cfg_combine": ([_c_ptr] * 8 + [_c_i32] * 5 + [_c_ptr], _c_i32),
     "pa_rope_packed": ([_c_ptr] * 5 + [_c_i32] * 5 + [_c_f32, _c_ptr], _c_i32),
+    "pa_linear_bf16": ([_c_ptr] * 4 + [_c_i32] * 3 + [_c_ptr], _c_i32),
 }
 
 
@@ -360,3 +361,29 @@ def selftest_wait_timeout(timeout_us: int = 1000, stream=None) -> None:
 
 def status_string(status: int) -> str:
     return load_library().pa_status_string(int(status)).decode()
+
+
+def linear_bf16(x: torch.Tensor, w: torch.Tensor, bias: Optional[torch.Tensor] = None,
+                out: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """y = x w^T + bias (pa_linear_bf16); x [M, K], w [N, K], bias [N], bf16."""
+    lib = load_library()
+    _need(x, "x", torch.bfloat16, 2)
+    _need(w, "w", torch.bfloat16, 2)
+    M, K = x.shape
+    N = w.shape[0]
+    if w.shape[1] != K:
+        raise ValueError(f"w must be [N, {K}], got {tuple(w.shape)}")
+    if bias is not None:
+        _need(bias, "bias", torch.bfloat16, 1)
+        if bias.shape[0] != N:
+            raise ValueError("bias must be [N]")
+    if out is None:
+        out = torch.empty(M, N, dtype=torch.bfloat16, device=x.device)
+    _need(out, "out", torch.bfloat16, 2)
+    if tuple(out.shape) != (M, N):
+        raise ValueError("out must be [M, N]")
+    st = lib.pa_linear_bf16(x.data_ptr(), w.data_ptr(),
+                            bias.data_ptr() if bias is not None else None, out.data_ptr(),
+                            M, N, K, _stream(stream))
+    _check("pa_linear_bf16", st)
+    return out

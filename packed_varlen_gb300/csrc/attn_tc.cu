@@ -39,6 +39,7 @@
 #include "internal.h"
 #include "sched.cuh"
 #include "tc_ptx.cuh"
+#include "tma_map.h"
 
 namespace pa {
 namespace {
@@ -506,28 +507,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
 }
 
-typedef CUresult (*EncodeTiledFn)(CUtensorMap *, CUtensorMapDataType, cuuint32_t, void *,
-                                  const cuuint64_t *, const cuuint64_t *, const cuuint32_t *,
-                                  const cuuint32_t *, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-  static EncodeTiledFn fn = nullptr;
-  if (fn == nullptr) {
-    void *ptr = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000,
-                                         cudaEnableDefault, &q) == cudaSuccess &&
-        q == cudaDriverEntryPointSuccess)
-      fn = reinterpret_cast<EncodeTiledFn>(ptr);
-  }
-  return fn;
-}
-
 // [rows, H, D] bf16 viewed as a 3-D tensor (D, H, rows); box 64 x 1 x 128
 // with 128-byte swizzle: one 128-row, 64-column half tile per load.
 bool make_map(CUtensorMap *map, const void *ptr, int rows, int H, int D) {
-  EncodeTiledFn enc = encode_fn();
+  EncodeTiledFn enc = tensor_map_encoder();
   if (enc == nullptr) return false;
   const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
                               static_cast<cuuint64_t>(rows > 0 ? rows : 1)};

@@ -1,0 +1,302 @@
+// Batch-invariant packed-M linear layer on the 5th-generation tensor cores:
+//
+//   y[m, n] = sum_k x[m, k] * w[n, k]  (+ bias[n])
+//
+// with bf16 x, w, bias and y and fp32 accumulation.  The packed path runs
+// the projections of every request at once on the flat [total_tokens, C]
+// activations, and its batched and serial outputs are bit-identical because
+// these GEMMs give a row the same result whatever the packed M is ("feat:
+// Support dynamic batching for heterogeneous diffusion requests", packed
+// varlen step batching: Setup, Determinism, and Notes, item 1).
+//
+// Batch invariance by construction: one tile shape (128 x 256 x 64) for every
+// M, no split-K, K walked in the same order in every tile, and an epilogue
+// that treats each row alone.  A row's result therefore depends only on its
+// own x row, w and bias: packed or alone, at any row offset, the bits agree.
+//
+// Kernel: persistent, one CTA per SM, six warps.  Warp 0 issues TMA loads of
+// x and w tiles (128-byte swizzle) into a kStages-deep shared-memory ring;
+// warp 1 issues tcgen05.mma (M = 128, N = 256, K = 16) into one of two TMEM
+// accumulators (2 x 256 fp32 columns); warps 2-5 drain a finished accumulator
+// (each warp its TMEM lane quadrant), add the bias, round to bf16 and store,
+// while the MMA warp fills the other accumulator.  Tiles go round-robin over
+// the CTAs, N-block fastest, so a wave of CTAs shares x rows and w stays in
+// L2.  Every wait is bounded; a timeout records PA_DEVICE_ERR_TIMEOUT.
+#include <cuda_bf16.h>
+#include <stdint.h>
+
+#include "internal.h"
+#include "sched.cuh"
+#include "tc_ptx.cuh"
+#include "tma_map.h"
+
+namespace pa {
+namespace {
+
+using namespace tc;
+
+constexpr int kBM = 128, kBN = 256, kBK = 64;
+constexpr int kStages = 4;
+constexpr int kThreads = 192;                   // TMA, MMA, 4 epilogue warps
+constexpr long long kWaitLimit = 4000000000LL;  // clock cycles (~2 s)
+constexpr long long kDrainLimit = 400000000LL;  // teardown after an abort (~0.2 s)
+
+struct GemmCfg {
+  static constexpr int kABytes = kBM * kBK * 2;          // 16 KB: 128 rows x 128 B
+  static constexpr int kBBytes = kBN * kBK * 2;          // 32 KB: 256 rows x 128 B
+  static constexpr int kStageBytes = kABytes + kBBytes;
+  static constexpr int kBarOff = kStages * kStageBytes;
+  static constexpr int kFull = 0, kEmpty = kStages, kAccFull = 2 * kStages,
+                       kAccEmpty = 2 * kStages + 2, kFinal = 2 * kStages + 4;
+  static constexpr int kNumBars = 2 * kStages + 5;
+  static constexpr int kMiscOff = kBarOff + kNumBars * 8;  // tmem base, abort flag
+  static constexpr int kSmemBytes = kMiscOff + 16;
+  static constexpr uint32_t kTmemCols = 2 * kBN;
+  // A (x) and B (w) both K-major
+  static constexpr uint32_t kIdesc = idesc_bf16_f32(kBM, kBN, false);
+};
+static_assert(GemmCfg::kSmemBytes <= 232448, "shared memory plan exceeds the per-CTA limit");
+
+struct GemmParams {
+  const __nv_bfloat16 *bias;  // [N] or nullptr
+  __nv_bfloat16 *y;           // [M, N]
+  int M, N, K;
+  int tiles_n, n_tiles, k_blocks;
+  int32_t *status;
+};
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+__global__ void __launch_bounds__(kThreads, 1)
+    linear_bf16_kernel(const __grid_constant__ CUtensorMap tm_x,
+                       const __grid_constant__ CUtensorMap tm_w, const GemmParams p) {
+  using C = GemmCfg;
+  extern __shared__ uint8_t smem_raw[];
+  // 128-byte swizzle atoms need a 1024-byte aligned base
+  const uint32_t base = smem_u32(smem_raw);
+  if (base & 1023u) {
+    if (threadIdx.x == 0) record_error(p.status, PA_DEVICE_ERR_SMEM_ALIGN);
+    return;
+  }
+  auto bar = [&](int i) -> uint32_t { return base + C::kBarOff + 8u * i; };
+  uint32_t *tmem_ptr = reinterpret_cast<uint32_t *>(smem_raw + C::kMiscOff);
+  volatile int32_t *abort_flag = reinterpret_cast<volatile int32_t *>(smem_raw + C::kMiscOff + 4);
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+
+  if (tid == 0) {
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(bar(C::kFull + s), 1);
+      mbar_init(bar(C::kEmpty + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(bar(C::kAccFull + b), 1);
+      mbar_init(bar(C::kAccEmpty + b), 128);
+    }
+    mbar_init(bar(C::kFinal), 1);
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) tmem_alloc(base + C::kMiscOff, C::kTmemCols);
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  const uint32_t tmem = *tmem_ptr;
+
+  if (warp == 0) {
+    // ================= TMA producer =================
+    if (lane == 0) {
+      tma_prefetch_desc(&tm_x);
+      tma_prefetch_desc(&tm_w);
+      uint32_t loads = 0;
+      bool ok = true;
+      for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
+        const int m0 = (t / p.tiles_n) * kBM, n0 = (t % p.tiles_n) * kBN;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          const uint32_t s = loads % kStages, use = loads / kStages;
+          if (!bounded_wait(bar(C::kEmpty + s), (use & 1u) ^ 1u, abort_flag, p.status,
+                            kWaitLimit)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(bar(C::kFull + s), C::kStageBytes);
+          const uint32_t dst = base + s * C::kStageBytes;
+          tma_load_2d(dst, &tm_x, bar(C::kFull + s), kb * kBK, m0);
+          tma_load_2d(dst + C::kABytes, &tm_w, bar(C::kFull + s), kb * kBK, n0);
+          ++loads;
+        }
+      }
+      if (!ok) {
+        // give the copies already issued a bounded chance to land
+        for (uint32_t s = 0; s < static_cast<uint32_t>(kStages) && s < loads; ++s) {
+          const uint32_t n = (loads - s + kStages - 1) / kStages;  // loads into slot s
+          drain_wait(bar(C::kFull + s), (n - 1) & 1u, kDrainLimit);
+        }
+      }
+    }
+  } else if (warp == 1) {
+    // ================= MMA issuer =================
+    if (lane == 0) {
+      uint32_t uses = 0, tiles_done = 0;
+      bool ok = true, issued = false;
+      // descriptors advance by adding the byte offset >> 4 to the start
+      // address field; every operand lies below 256 KB, so nothing carries
+      const uint64_t adesc0 = sdesc_sw128(base, 16, 1024);
+      const uint64_t bdesc0 = sdesc_sw128(base + C::kABytes, 16, 1024);
+      for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x, ++tiles_done) {
+        const uint32_t buf = tiles_done & 1u, buse = tiles_done >> 1;
+        if (!bounded_wait(bar(C::kAccEmpty + buf), (buse & 1u) ^ 1u, abort_flag, p.status,
+                          kWaitLimit)) {
+          ok = false;
+          break;
+        }
+        fence_after_sync();
+        const uint32_t d = tmem + buf * kBN;
+        for (int kb = 0; kb < p.k_blocks; ++kb) {
+          const uint32_t s = uses % kStages;
+          if (!bounded_wait(bar(C::kFull + s), (uses / kStages) & 1u, abort_flag, p.status,
+                            kWaitLimit)) {
+            ok = false;
+            break;
+          }
+          fence_after_sync();
+          const uint64_t a = adesc0 + ((s * C::kStageBytes) >> 4);
+          const uint64_t b = bdesc0 + ((s * C::kStageBytes) >> 4);
+#pragma unroll
+          for (int kk = 0; kk < kBK / 16; ++kk)
+            mma_ss(d, a + ((kk * 32) >> 4), b + ((kk * 32) >> 4), C::kIdesc,
+                   (kb > 0 || kk > 0) ? 1u : 0u);
+          issued = true;
+          mma_commit(bar(C::kEmpty + s));   // the slot is free once these MMAs finish
+          ++uses;
+        }
+        if (!ok) break;
+        mma_commit(bar(C::kAccFull + buf));
+      }
+      // every MMA issued so far has finished before TMEM is released
+      if (issued) {
+        mma_commit(bar(C::kFinal));
+        drain_wait(bar(C::kFinal), 0, kWaitLimit);
+      }
+    }
+    __syncwarp();
+  } else {
+    // ================= epilogue: warps 2..5, TMEM lane quadrant warp % 4 =========
+    const int quad = warp & 3;
+    const int r = quad * 32 + lane;
+    const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
+    uint32_t tiles_done = 0;
+    for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++tiles_done) {
+      const uint32_t buf = tiles_done & 1u, buse = tiles_done >> 1;
+      const bool ok = bounded_wait(bar(C::kAccFull + buf), buse & 1u, abort_flag, p.status,
+                                   kWaitLimit);
+      if (!__all_sync(0xffffffffu, ok)) break;
+      fence_after_sync();
+      const int m = (t / p.tiles_n) * kBM + r;
+      const int n0 = (t % p.tiles_n) * kBN;
+      const bool row_ok = m < p.M;
+      __nv_bfloat16 *yrow = p.y + static_cast<int64_t>(row_ok ? m : 0) * p.N;
+#pragma unroll 1
+      for (int c = 0; c < kBN / 32; c += 2) {
+        uint32_t a0[32], a1[32];
+        tmem_ld32(lane_base + buf * kBN + c * 32, a0);
+        tmem_ld32(lane_base + buf * kBN + (c + 1) * 32, a1);
+        tmem_wait_ld();
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+          const uint32_t *acc = h == 0 ? a0 : a1;
+          const int col = n0 + (c + h) * 32;
+          if (!row_ok || col >= p.N) continue;
+#pragma unroll
+          for (int v = 0; v < 4; ++v) {
+            const int c8 = col + 8 * v;
+            if (c8 >= p.N) break;   // N is a multiple of 8
+            float f[8];
+#pragma unroll
+            for (int e = 0; e < 8; ++e) f[e] = __uint_as_float(acc[8 * v + e]);
+            if (p.bias) {
+              const uint4 bv = __ldg(reinterpret_cast<const uint4 *>(p.bias + c8));
+              f[0] += bf16_lo(bv.x); f[1] += bf16_hi(bv.x);
+              f[2] += bf16_lo(bv.y); f[3] += bf16_hi(bv.y);
+              f[4] += bf16_lo(bv.z); f[5] += bf16_hi(bv.z);
+              f[6] += bf16_lo(bv.w); f[7] += bf16_hi(bv.w);
+            }
+            uint4 o;
+            o.x = pack_bf16x2(f[0], f[1]);
+            o.y = pack_bf16x2(f[2], f[3]);
+            o.z = pack_bf16x2(f[4], f[5]);
+            o.w = pack_bf16x2(f[6], f[7]);
+            *reinterpret_cast<uint4 *>(yrow + c8) = o;
+          }
+        }
+      }
+      fence_before_sync();
+      mbar_arrive(bar(C::kAccEmpty + buf));   // the MMA warp may refill this accumulator
+    }
+  }
+
+  // ---- teardown -------------------------------------------------------------
+  fence_before_sync();
+  __syncthreads();
+  fence_after_sync();
+  if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
+}
+
+// [rows, K] bf16 row-major as a 2-D tensor (K, rows); box 64 x box_rows with
+// 128-byte swizzle: one K-block of box_rows rows per load.  Rows and columns
+// past the end read as zero.
+bool make_map_2d(CUtensorMap *map, const void *ptr, int rows, int K, int box_rows) {
+  EncodeTiledFn enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(K), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(K) * 2};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(ptr), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+}  // namespace
+}  // namespace pa
+
+extern "C" pa_status pa_linear_bf16(const void *x, const void *w, const void *bias, void *y,
+                                    int32_t M, int32_t N, int32_t K, pa_stream_t stream) {
+  using namespace pa;
+  if (M < 0 || N < 1 || K < 1 || !w) return PA_ERR_INVALID_ARG;
+  if (M == 0) return PA_OK;   // nothing to read or write; x and y may be NULL
+  if (!x || !y) return PA_ERR_INVALID_ARG;
+  if ((K & 7) != 0 || (N & 7) != 0 || !aligned16(x) || !aligned16(w) || !aligned16(y) ||
+      (bias && !aligned16(bias)))
+    return PA_ERR_MISALIGNED;
+  int32_t *status;
+  int sms;
+  cudaError_t e = device_context(&status, &sms);
+  if (e != cudaSuccess) return from_cuda(e);
+  CUtensorMap mx, mw;
+  if (!make_map_2d(&mx, x, M, K, kBM) || !make_map_2d(&mw, w, N, K, kBN))
+    return from_cuda(cudaErrorInvalidValue);
+  GemmParams p;
+  p.bias = static_cast<const __nv_bfloat16 *>(bias);
+  p.y = static_cast<__nv_bfloat16 *>(y);
+  p.M = M;
+  p.N = N;
+  p.K = K;
+  p.tiles_n = (N + kBN - 1) / kBN;
+  const int64_t tiles = static_cast<int64_t>((M + kBM - 1) / kBM) * p.tiles_n;
+  if (tiles > 0x7fffffff) return PA_ERR_UNSUPPORTED;
+  p.n_tiles = static_cast<int>(tiles);
+  p.k_blocks = (K + kBK - 1) / kBK;
+  p.status = status;
+  static unsigned long long configured = 0;
+  e = set_smem_once(reinterpret_cast<const void *>(linear_bf16_kernel), GemmCfg::kSmemBytes,
+                    configured);
+  if (e != cudaSuccess) return from_cuda(e);
+  const int grid = p.n_tiles < sms ? p.n_tiles : sms;
+  linear_bf16_kernel<<<grid, kThreads, GemmCfg::kSmemBytes,
+                       reinterpret_cast<cudaStream_t>(stream)>>>(mx, mw, p);
+  return from_cuda(cudaGetLastError());
+}

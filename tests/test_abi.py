@@ -32,7 +32,7 @@ def test_header_declares_expected_entry_points():
               "pa_pack", "pa_unpack", "pa_varlen_work_order", "pa_varlen_num_work_items",
               "pa_get_device_status", "pa_status_string", "pa_cfg_combine",
               "pa_last_cuda_error", "pa_selftest_wait_timeout", "pa_rope_packed",
-              "pa_block_window_attn_fwd_f32"]:
+              "pa_block_window_attn_fwd_f32", "pa_linear_bf16"]:
         assert n in names
 
 
@@ -139,3 +139,20 @@ def test_rope_host_checks(lib):
         bad = list(ok)
         bad[i] = v
         assert lib.pa_rope_packed(*bad) == code, (i, v)
+
+
+def test_linear_host_checks(lib):
+    # every call has exactly one broken field, so nothing reaches the device
+    ok = [A, A, None, A, 300, 512, 3072, None]
+    for i, v, code in [(0, None, 1), (1, None, 1), (3, None, 1), (4, -1, 1), (5, 0, 1),
+                       (6, 0, 1), (5, 516, 3), (6, 3076, 3), (0, MIS, 3), (3, A + 2, 3),
+                       (2, MIS, 3)]:
+        bad = list(ok)
+        bad[i] = v
+        assert lib.pa_linear_bf16(*bad) == code, (i, v)
+    # M = 0 is a no-op that touches nothing; x and y may then be NULL
+    empty = list(ok)
+    empty[4] = 0
+    assert lib.pa_linear_bf16(*empty) == 0
+    empty[0] = empty[3] = None
+    assert lib.pa_linear_bf16(*empty) == 0

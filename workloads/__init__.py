@@ -267,6 +267,52 @@ def random_block_window(batch: int, n: int, H: int, D: int, block: int, seed: in
                                list(layers or [(0, 0)]), q, k, v, seed)
 
 
+@dataclass
+class LinearWorkload:
+    """A packed-M projection: x [M, K] (the flat tokens of every request),
+    w [N, K], bias [N]; `lengths` are the requests' row counts in x."""
+    name: str
+    lengths: List[int]
+    x: torch.Tensor
+    w: torch.Tensor
+    bias: Optional[torch.Tensor]
+    seed: int
+
+    @property
+    def M(self) -> int:
+        return self.x.shape[0]
+
+    @property
+    def N(self) -> int:
+        return self.w.shape[0]
+
+    @property
+    def K(self) -> int:
+        return self.x.shape[1]
+
+
+def linear_case(lengths: List[int], N: int, K: int, seed: int, bias: bool = True,
+                name: str = "linear") -> LinearWorkload:
+    """x ~ N(0, 1), w ~ N(0, 1/K) (unit-variance outputs), bias ~ N(0, 0.1^2),
+    all rounded to bf16."""
+    g = torch.Generator().manual_seed(seed)
+    M = int(sum(lengths))
+    x = _randn_bf16(g, (M, K))
+    w = (torch.randn(N, K, generator=g) / float(K) ** 0.5).to(torch.bfloat16)
+    b = (0.1 * torch.randn(N, generator=g)).to(torch.bfloat16) if bias else None
+    return LinearWorkload(name, list(lengths), x, w, b, seed)
+
+
+def mmdit_projection(kind: str = "qkv", seed: int = 2) -> LinearWorkload:
+    """A projection of the mixed-resolution MMDiT batch: x is the batch's
+    packed [T, 3072] hidden states (24 heads x 128); "qkv" multiplies by the
+    fused [9216, 3072] QKV weight, "out" by the [3072, 3072] output weight."""
+    g = torch.Generator().manual_seed(seed)
+    L = lengths_mixed_res(g)
+    N = {"qkv": 3 * 3072, "out": 3072}[kind]
+    return linear_case(L, N, 3072, seed + 2000, bias=True, name=f"mmdit_{kind}_projection")
+
+
 VARLEN_CONFIGS = {
     "tiny": tiny,
     "mixed_res_mmdit": mixed_res,
