@@ -14,14 +14,20 @@
 // that treats each row alone.  A row's result therefore depends only on its
 // own x row, w and bias: packed or alone, at any row offset, the bits agree.
 //
-// Kernel: persistent, one CTA per SM, six warps.  Warp 0 issues TMA loads of
-// x and w tiles (128-byte swizzle) into a kStages-deep shared-memory ring;
-// warp 1 issues tcgen05.mma (M = 128, N = 256, K = 16) into one of two TMEM
-// accumulators (2 x 256 fp32 columns); warps 2-5 drain a finished accumulator
-// (each warp its TMEM lane quadrant), add the bias, round to bf16 and store,
-// while the MMA warp fills the other accumulator.  Tiles go round-robin over
-// the CTAs, N-block fastest, so a wave of CTAs shares x rows and w stays in
-// L2.  Every wait is bounded; a timeout records PA_DEVICE_ERR_TIMEOUT.
+// Kernel: persistent, one CTA per SM, CTAs in clusters of two, six warps.
+// The two CTAs of a cluster compute vertically adjacent 128 x 256 tiles of
+// the same w columns: each loads its own x tile and one half of the w tile,
+// and multicasts that half into both CTAs' shared memory, so every w byte
+// crosses from L2 once per pair (L2 bandwidth is what bounds a lone CTA).
+// Warp 0 issues the TMA loads (128-byte swizzle) into a kStages-deep ring;
+// warp 1 issues tcgen05.mma (M = 128, N = 256, K = 16, one CTA each) into one
+// of two TMEM accumulators (2 x 256 fp32 columns) and frees a ring slot in
+// both CTAs once its MMAs are done (a slot holds the peer's w half too);
+// warps 2-5 drain a finished accumulator (each warp its TMEM lane quadrant),
+// add the bias, round to bf16 and store, while the MMA warp fills the other
+// accumulator.  Tile pairs go round-robin over the clusters, N-block fastest,
+// so a wave shares x rows and w stays in L2.  Every wait is bounded; a
+// timeout records PA_DEVICE_ERR_TIMEOUT.
 #include <cuda_bf16.h>
 #include <stdint.h>
 
@@ -37,6 +43,8 @@ using namespace tc;
 
 constexpr int kBM = 128, kBN = 256, kBK = 64;
 constexpr int kStages = 4;
+constexpr int kCluster = 2;                     // CTAs sharing one w tile
+constexpr uint16_t kPairMask = 0x3;
 constexpr int kThreads = 192;                   // TMA, MMA, 4 epilogue warps
 constexpr long long kWaitLimit = 4000000000LL;  // clock cycles (~2 s)
 constexpr long long kDrainLimit = 400000000LL;  // teardown after an abort (~0.2 s)
@@ -61,14 +69,14 @@ struct GemmParams {
   const __nv_bfloat16 *bias;  // [N] or nullptr
   __nv_bfloat16 *y;           // [M, N]
   int M, N, K;
-  int tiles_n, n_tiles, k_blocks;
+  int tiles_n, n_pairs, k_blocks;   // n_pairs: (pair of 128-row blocks, N block)
   int32_t *status;
 };
 
 __device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
 __device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
 
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     linear_bf16_kernel(const __grid_constant__ CUtensorMap tm_x,
                        const __grid_constant__ CUtensorMap tm_w, const GemmParams p) {
   using C = GemmCfg;
@@ -87,7 +95,7 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (tid == 0) {
     for (int s = 0; s < kStages; ++s) {
       mbar_init(bar(C::kFull + s), 1);
-      mbar_init(bar(C::kEmpty + s), 1);
+      mbar_init(bar(C::kEmpty + s), kCluster);   // both CTAs' MMAs read the slot
     }
     for (int b = 0; b < 2; ++b) {
       mbar_init(bar(C::kAccFull + b), 1);
@@ -99,9 +107,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
   if (warp == 1) tmem_alloc(base + C::kMiscOff, C::kTmemCols);
   fence_before_sync();
-  __syncthreads();
+  __syncwarp();     // the cluster barrier is warp-aligned
+  cluster_sync();   // barriers of both CTAs initialised before any remote use
   fence_after_sync();
   const uint32_t tmem = *tmem_ptr;
+  const uint32_t rank = cluster_ctarank();
+  const int cl = blockIdx.x / kCluster, n_cl = gridDim.x / kCluster;
 
   if (warp == 0) {
     // ================= TMA producer =================
@@ -110,8 +121,9 @@ __global__ void __launch_bounds__(kThreads, 1)
       tma_prefetch_desc(&tm_w);
       uint32_t loads = 0;
       bool ok = true;
-      for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x) {
-        const int m0 = (t / p.tiles_n) * kBM, n0 = (t % p.tiles_n) * kBN;
+      for (int tp = cl; tp < p.n_pairs && ok; tp += n_cl) {
+        const int m0 = ((tp / p.tiles_n) * kCluster + rank) * kBM;
+        const int n0 = (tp % p.tiles_n) * kBN + rank * (kBN / kCluster);
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           const uint32_t s = loads % kStages, use = loads / kStages;
           if (!bounded_wait(bar(C::kEmpty + s), (use & 1u) ^ 1u, abort_flag, p.status,
@@ -122,7 +134,9 @@ __global__ void __launch_bounds__(kThreads, 1)
           mbar_arrive_expect_tx(bar(C::kFull + s), C::kStageBytes);
           const uint32_t dst = base + s * C::kStageBytes;
           tma_load_2d(dst, &tm_x, bar(C::kFull + s), kb * kBK, m0);
-          tma_load_2d(dst + C::kABytes, &tm_w, bar(C::kFull + s), kb * kBK, n0);
+          // this CTA's half of the w tile, into both CTAs of the pair
+          tma_load_2d_multicast(dst + C::kABytes + rank * (C::kBBytes / kCluster), &tm_w,
+                                bar(C::kFull + s), kb * kBK, n0, kPairMask);
           ++loads;
         }
       }
@@ -143,7 +157,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       // address field; every operand lies below 256 KB, so nothing carries
       const uint64_t adesc0 = sdesc_sw128(base, 16, 1024);
       const uint64_t bdesc0 = sdesc_sw128(base + C::kABytes, 16, 1024);
-      for (int t = blockIdx.x; t < p.n_tiles && ok; t += gridDim.x, ++tiles_done) {
+      for (int tp = cl; tp < p.n_pairs && ok; tp += n_cl, ++tiles_done) {
         const uint32_t buf = tiles_done & 1u, buse = tiles_done >> 1;
         if (!bounded_wait(bar(C::kAccEmpty + buf), (buse & 1u) ^ 1u, abort_flag, p.status,
                           kWaitLimit)) {
@@ -167,7 +181,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_ss(d, a + ((kk * 32) >> 4), b + ((kk * 32) >> 4), C::kIdesc,
                    (kb > 0 || kk > 0) ? 1u : 0u);
           issued = true;
-          mma_commit(bar(C::kEmpty + s));   // the slot is free once these MMAs finish
+          // the slot (with the peer's w half) is free once both CTAs' MMAs finish
+          mma_commit_multicast(bar(C::kEmpty + s), kPairMask);
           ++uses;
         }
         if (!ok) break;
@@ -186,14 +201,14 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int r = quad * 32 + lane;
     const uint32_t lane_base = tmem + (static_cast<uint32_t>(quad * 32) << 16);
     uint32_t tiles_done = 0;
-    for (int t = blockIdx.x; t < p.n_tiles; t += gridDim.x, ++tiles_done) {
+    for (int tp = cl; tp < p.n_pairs; tp += n_cl, ++tiles_done) {
       const uint32_t buf = tiles_done & 1u, buse = tiles_done >> 1;
       const bool ok = bounded_wait(bar(C::kAccFull + buf), buse & 1u, abort_flag, p.status,
                                    kWaitLimit);
       if (!__all_sync(0xffffffffu, ok)) break;
       fence_after_sync();
-      const int m = (t / p.tiles_n) * kBM + r;
-      const int n0 = (t % p.tiles_n) * kBN;
+      const int m = ((tp / p.tiles_n) * kCluster + rank) * kBM + r;
+      const int n0 = (tp % p.tiles_n) * kBN;
       const bool row_ok = m < p.M;
       __nv_bfloat16 *yrow = p.y + static_cast<int64_t>(row_ok ? m : 0) * p.N;
 #pragma unroll 1
@@ -236,8 +251,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 
   // ---- teardown -------------------------------------------------------------
+  // neither CTA leaves while the other may still write into its shared memory
+  // or arrive on its barriers
   fence_before_sync();
-  __syncthreads();
+  __syncwarp();     // the cluster barrier is warp-aligned
+  cluster_sync();
   fence_after_sync();
   if (warp == 1) tmem_dealloc(tmem, C::kTmemCols);
 }
@@ -277,7 +295,7 @@ extern "C" pa_status pa_linear_bf16(const void *x, const void *w, const void *bi
   cudaError_t e = device_context(&status, &sms);
   if (e != cudaSuccess) return from_cuda(e);
   CUtensorMap mx, mw;
-  if (!make_map_2d(&mx, x, M, K, kBM) || !make_map_2d(&mw, w, N, K, kBN))
+  if (!make_map_2d(&mx, x, M, K, kBM) || !make_map_2d(&mw, w, N, K, kBN / kCluster))
     return from_cuda(cudaErrorInvalidValue);
   GemmParams p;
   p.bias = static_cast<const __nv_bfloat16 *>(bias);
@@ -286,16 +304,19 @@ extern "C" pa_status pa_linear_bf16(const void *x, const void *w, const void *bi
   p.N = N;
   p.K = K;
   p.tiles_n = (N + kBN - 1) / kBN;
-  const int64_t tiles = static_cast<int64_t>((M + kBM - 1) / kBM) * p.tiles_n;
-  if (tiles > 0x7fffffff) return PA_ERR_UNSUPPORTED;
-  p.n_tiles = static_cast<int>(tiles);
+  const int64_t m_pairs = ((M + kBM - 1) / kBM + kCluster - 1) / kCluster;
+  const int64_t pairs = m_pairs * p.tiles_n;
+  if (pairs > 0x3fffffff) return PA_ERR_UNSUPPORTED;
+  p.n_pairs = static_cast<int>(pairs);
   p.k_blocks = (K + kBK - 1) / kBK;
   p.status = status;
   static unsigned long long configured = 0;
   e = set_smem_once(reinterpret_cast<const void *>(linear_bf16_kernel), GemmCfg::kSmemBytes,
                     configured);
   if (e != cudaSuccess) return from_cuda(e);
-  const int grid = p.n_tiles < sms ? p.n_tiles : sms;
+  // whole clusters, at most one CTA per SM
+  const int max_ctas = sms / kCluster * kCluster;
+  const int grid = kCluster * p.n_pairs < max_ctas ? kCluster * p.n_pairs : max_ctas;
   linear_bf16_kernel<<<grid, kThreads, GemmCfg::kSmemBytes,
                        reinterpret_cast<cudaStream_t>(stream)>>>(mx, mw, p);
   return from_cuda(cudaGetLastError());
