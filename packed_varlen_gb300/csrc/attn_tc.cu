@@ -6,19 +6,23 @@
 // varlen attention for mixfusion", Key changes; "feat: Support dynamic
 // batching for heterogeneous diffusion requests", AttentionMetadata).
 //
-// Design: one persistent CTA per SM, 10 warps.  A work item is 256 query
+// Design: one persistent CTA per SM, 11 warps.  A work item is 256 query
 // rows of one (sequence, head), held as two 128-row tiles Q0 and Q1 that share
 // every K/V tile loaded, so each K/V byte brought into shared memory feeds
 // twice the tensor-core work of a single-tile item.
 //   warp 0      TMA producer: Q0/Q1 once per item, then K0, V0, K1, V1, ...
 //               through a ring of shared-memory slots.
 //   warp 1      allocates TMEM (S0, S1, O0, O1: 128 columns each); lane 0
-//               issues tcgen05.mma in the order
-//                 S0_0 S1_0 | PV0_0 S0_1 PV1_0 S1_1 | PV0_1 S0_2 ...
+//               issues tile 0's tcgen05.mma in the order
+//                 S0_0 | PV0_0 S0_1 | PV0_1 S0_2 ...
+//   warp 10     lane 0 issues tile 1's in the same order.
 //               S = Q K^T with both operands in shared memory, fp32 into TMEM;
 //               O += P V with P (bf16) read from TMEM, V from shared memory.
 //               While one tile's softmax runs, the tensor core computes the
-//               other tile's PV and next S.
+//               other tile's PV and next S.  Two issuing threads keep the
+//               tensor pipe fed: one thread's waits, fences and commits
+//               between 128-wide MMA groups leave the pipe idle about a
+//               third of the time.
 //   warps 2..5  softmax of tile 0, one thread per query row (TMEM lane);
 //   warps 6..9  softmax of tile 1.  Each thread reads its row of S, runs the
 //               online softmax in fp32 (exp2 with the scale folded in),
@@ -26,7 +30,8 @@
 //               rescales O in TMEM only when the row maximum grew by more
 //               than 2^8, and finally normalises O and stores bf16 rows.
 // P overwrites S in place: the MMA that next writes that S buffer is issued
-// after the PV that reads P, and tcgen05 MMAs of one CTA execute in order.
+// after the PV that reads P by the same thread, and one thread's tcgen05
+// MMAs execute in order.
 // Every output row is computed by one CTA in a fixed key-tile order that
 // depends only on its own sequence, so results do not depend on the rest of
 // the batch.  Key columns past the sequence end are masked to -inf (P = 0);
@@ -48,7 +53,8 @@ using namespace tc;
 
 constexpr int kTile = 128;          // rows of a Q tile, keys of a K/V tile
 constexpr int kItemRows = 256;      // query rows per work item (two tiles)
-constexpr int kThreads = 320;       // producer, MMA, 2 x 4 softmax warps
+constexpr int kThreads = 352;       // producer, 2 MMA issuers, 2 x 4 softmax warps
+constexpr int kMmaWarp1 = kThreads / 32 - 1;   // issuer of tile 1
 constexpr long long kWaitLimit = 4000000000LL;  // clock cycles (~2 s)
 constexpr long long kDrainLimit = 400000000LL;  // teardown after an abort (~0.2 s)
 constexpr float kRescaleThreshold = 8.0f;       // log2 units
@@ -67,8 +73,8 @@ struct Cfg {
   static constexpr int kBarOff = kRingOff + kSlots * kTileBytes;
   // barriers: per Q tile t an S-full, a P-ready and an O-full barrier
   static constexpr int kQFull = 0, kQEmpty = 1, kSFull = 2, kPReady = 4, kOFull = 6,
-                       kFinal = 8, kSlotFull = 9, kSlotEmpty = 9 + kSlots;
-  static constexpr int kNumBars = 9 + 2 * kSlots;
+                       kFinal = 8, kTurn = 10, kSlotFull = 12, kSlotEmpty = 12 + kSlots;
+  static constexpr int kNumBars = 12 + 2 * kSlots;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;   // tmem base, abort flag
   static constexpr int kSchedOff = (kMiscOff + 16 + 127) / 128 * 128;
   static constexpr int kSmemBytes = kSchedOff + (2 * kMaxSeqs + 1) * 4;
@@ -156,16 +162,19 @@ __global__ void __launch_bounds__(kThreads, 1)
   // ---- set-up: barriers, TMEM, work list --------------------------------
   if (tid == 0) {
     mbar_init(bar(C::kQFull), 1);
-    mbar_init(bar(C::kQEmpty), 1);
+    mbar_init(bar(C::kQEmpty), 2);   // one arrival per MMA issuer
     for (int t = 0; t < 2; ++t) {
       mbar_init(bar(C::kSFull + t), 1);
       mbar_init(bar(C::kPReady + t), 128);
       mbar_init(bar(C::kOFull + t), 1);
     }
-    mbar_init(bar(C::kFinal), 1);
+    mbar_init(bar(C::kFinal + 0), 1);
+    mbar_init(bar(C::kFinal + 1), 1);
+    mbar_init(bar(C::kTurn + 0), 1);
+    mbar_init(bar(C::kTurn + 1), 1);
     for (int s = 0; s < C::kSlots; ++s) {
       mbar_init(bar(C::kSlotFull + s), 1);
-      mbar_init(bar(C::kSlotEmpty + s), 1);
+      mbar_init(bar(C::kSlotEmpty + s), 2);   // one arrival per MMA issuer
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -235,11 +244,16 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (q_loads) drain_wait(bar(C::kQFull), (q_loads - 1) & 1u, kDrainLimit);
       }
     }
-  } else if (warp == 1) {
-    // ================= MMA issuer =================
+  } else if (warp == 1 || warp == kMmaWarp1) {
+    // ================= MMA issuers: warp 1 for tile 0, the last warp for tile 1 ====
+    // Each issuer walks the same items and the same ring slots; it issues its
+    // own tile's MMAs in the order S_0 | PV_0 S_1 | PV_1 S_2 ... and frees a
+    // slot (or the Q buffer) with one arrival on a two-arrival barrier: a
+    // commit once its MMAs reading the slot are done, or a plain arrive when
+    // its tile is absent from the item.
+    const int t = warp == 1 ? 0 : 1;
     if (lane == 0) {
-      uint32_t q_uses = 0, slot_uses = 0, issued = 0;
-      uint32_t p_waits[2] = {0, 0};
+      uint32_t q_uses = 0, slot_uses = 0, issued = 0, p_waits = 0;
       bool ok = true;
       // next ring slot in consumption order, once its load has landed
       auto wait_slot = [&](uint32_t &s) -> bool {
@@ -250,99 +264,121 @@ __global__ void __launch_bounds__(kThreads, 1)
       // S_t = Q_t K^T into S buffer t (Q/K K-major, SBO = 8 rows x 128 B)
       // (descriptors advance by adding the byte offset >> 4 to the start
       // address field; every operand lies below 256 KB, so nothing carries)
-      const uint64_t qdesc0 = sdesc_sw128(sQ, 16, 1024);
+      const uint64_t qdesc0 = sdesc_sw128(sQ, 16, 1024) + ((t * C::kTileBytes) >> 4);
       const uint64_t kdesc0 = sdesc_sw128(sRing, 16, 1024);
       const uint64_t vdesc0 = sdesc_sw128(sRing, C::kVLbo, 1024);
-      const uint32_t d_s = tmem + C::kColS, d_o = tmem + C::kColO;
-      auto issue_s = [&](int t, uint32_t slot) {
-        const uint64_t a0 = qdesc0 + ((t * C::kTileBytes) >> 4);
+      const uint32_t d_s = tmem + C::kColS + t * kTile, d_o = tmem + C::kColO + t * D;
+      auto issue_s = [&](uint32_t slot) {
         const uint64_t b0 = kdesc0 + ((slot * C::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * C::kHalfBytes + (kk & 3) * 32) >> 4;
-          mma_ss(d_s + t * kTile, a0 + off, b0 + off, C::kIdescS, kk > 0 ? 1u : 0u);
+          mma_ss(d_s, qdesc0 + off, b0 + off, C::kIdescS, kk > 0 ? 1u : 0u);
         }
-        mma_commit(bar(C::kSFull + t));
       };
-      // O_t += P_t V once tile t's softmax has written P_t
-      auto issue_pv = [&](int t, uint32_t slot, bool first) -> bool {
-        if (!bounded_wait(bar(C::kPReady + t), p_waits[t] & 1u, abort_flag, p.status,
-                          kWaitLimit))
-          return false;
-        ++p_waits[t];
-        fence_after_sync();
+      // O_t += P_t V (P_t is in the first 64 columns of the S buffer)
+      auto issue_pv = [&](uint32_t slot, bool first) {
         const uint64_t b0 = vdesc0 + ((slot * C::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
-          mma_ts(d_o + t * D, d_s + t * kTile + kk * 8, b0 + ((kk * 16 * 128) >> 4), C::kIdescO,
+          mma_ts(d_o, d_s + kk * 8, b0 + ((kk * 16 * 128) >> 4), C::kIdescO,
                  (first && kk == 0) ? 0u : 1u);
         }
-        return true;
+      };
+      // The two issuers take turns group by group (S0_0, S1_0, [PV0_0 S0_1],
+      // [PV1_0 S1_1], ...), so the tensor pipe sees the single-thread order
+      // that staggers the two tiles; each thread finishes its waits before
+      // taking the turn and commits after passing it on.
+      uint32_t turns = 0;
+      auto take_turn = [&]() -> bool {
+        const uint32_t parity = t == 0 ? ((turns & 1u) ^ 1u) : (turns & 1u);
+        return bounded_wait(bar(C::kTurn + t), parity, abort_flag, p.status, kWaitLimit);
+      };
+      auto pass_turn = [&]() {
+        ++turns;
+        mbar_arrive(bar(C::kTurn + (1 - t)));
       };
       for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
         const ItemInfo it = item_info(p, order, prefix, i);
         if (it.nk == 0) continue;
-        const bool two = it.rows > kTile;
+        const bool mine = it.rows > t * kTile;   // this issuer's tile is in the item
+        // release a slot / the Q buffer: after this tile's MMAs, or at once
+        auto release = [&](uint32_t b) {
+          if (mine)
+            mma_commit(b);
+          else
+            mbar_arrive(b);
+        };
         if (!bounded_wait(bar(C::kQFull), q_uses & 1u, abort_flag, p.status, kWaitLimit)) {
           ok = false;
           break;
         }
         ++q_uses;
-        // prologue: S0_0 (and S1_0) from K_0
+        // prologue: S_0 from K_0
         uint32_t sk;
-        if (!wait_slot(sk)) {
+        if (!wait_slot(sk) || !take_turn()) {
           ok = false;
           break;
         }
-        issue_s(0, sk);
-        if (two) issue_s(1, sk);
-        issued = 1;
-        mma_commit(bar(C::kSlotEmpty + sk));
+        if (mine) {
+          issue_s(sk);
+          issued = 1;
+        }
+        pass_turn();
+        if (mine) mma_commit(bar(C::kSFull + t));
+        release(bar(C::kSlotEmpty + sk));
         ++slot_uses;
-        if (it.nk == 1) mma_commit(bar(C::kQEmpty));
+        if (it.nk == 1) release(bar(C::kQEmpty));
         for (int j = 0; j < it.nk && ok; ++j) {
-          uint32_t sv;
+          const bool more = j + 1 < it.nk;
+          uint32_t sv, sk2 = 0;
           if (!wait_slot(sv)) {
             ok = false;
             break;
           }
           ++slot_uses;
-          const bool more = j + 1 < it.nk;
-          uint32_t sk2 = 0;
-          // tile 0: PV0_j, then S0_{j+1} (after the PV that reads P0 from S0)
-          if (!issue_pv(0, sv, j == 0)) {
+          if (more && !wait_slot(sk2)) {
             ok = false;
             break;
           }
-          if (!more) mma_commit(bar(C::kOFull + 0));
-          if (more) {
-            if (!wait_slot(sk2)) {
+          // P_j written by this tile's softmax
+          if (mine) {
+            if (!bounded_wait(bar(C::kPReady + t), p_waits & 1u, abort_flag, p.status,
+                              kWaitLimit)) {
               ok = false;
               break;
             }
-            issue_s(0, sk2);
+            ++p_waits;
+            fence_after_sync();
           }
-          // tile 1: PV1_j, then S1_{j+1}
-          if (two) {
-            if (!issue_pv(1, sv, j == 0)) {
-              ok = false;
-              break;
-            }
-            if (!more) mma_commit(bar(C::kOFull + 1));
+          if (!take_turn()) {
+            ok = false;
+            break;
           }
-          mma_commit(bar(C::kSlotEmpty + sv));
+          // PV_j, then S_{j+1} (after the PV that reads P from the S buffer)
+          if (mine) {
+            issue_pv(sv, j == 0);
+            if (more) issue_s(sk2);
+          }
+          pass_turn();
+          if (mine) {
+            if (more)
+              mma_commit(bar(C::kSFull + t));
+            else
+              mma_commit(bar(C::kOFull + t));
+          }
+          release(bar(C::kSlotEmpty + sv));
           if (more) {
-            if (two) issue_s(1, sk2);
-            mma_commit(bar(C::kSlotEmpty + sk2));
+            release(bar(C::kSlotEmpty + sk2));
             ++slot_uses;
-            if (j + 2 == it.nk) mma_commit(bar(C::kQEmpty));
+            if (j + 2 == it.nk) release(bar(C::kQEmpty));
           }
         }
       }
-      // every MMA issued so far has finished before TMEM is released
+      // every MMA this thread issued has finished before TMEM is released
       if (issued) {
-        mma_commit(bar(C::kFinal));
-        drain_wait(bar(C::kFinal), 0, kWaitLimit);
+        mma_commit(bar(C::kFinal + t));
+        drain_wait(bar(C::kFinal + t), 0, kWaitLimit);
       }
     }
     __syncwarp();
