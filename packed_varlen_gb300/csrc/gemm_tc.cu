@@ -168,12 +168,13 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
         const uint32_t d = tmem + buf * kBN;
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           const uint32_t s = uses % kStages;
+          // the TMA bytes completed on this barrier are visible to the MMA
+          // once the wait returns (no TMEM hand-off, so no tcgen05 fence)
           if (!bounded_wait(bar(C::kFull + s), (uses / kStages) & 1u, abort_flag, p.status,
                             kWaitLimit)) {
             ok = false;
             break;
           }
-          fence_after_sync();
           const uint64_t a = adesc0 + ((s * C::kStageBytes) >> 4);
           const uint64_t b = bdesc0 + ((s * C::kStageBytes) >> 4);
 #pragma unroll
