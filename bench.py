@@ -92,19 +92,28 @@ def _kernel_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def _profiled_traffic(digest: str):
-    """DRAM bytes per launch of the attention kernel from the committed ncu
-    summary, if it was taken on the current kernel sources."""
+def _profiled(digest: str):
+    """Figures of the attention kernel from the committed ncu summary (DRAM
+    bytes per launch, tensor-pipe utilisation, DRAM GB/s), if it was taken on
+    the current kernel sources; else an empty dict."""
     path = os.path.join(ROOT, "profiles", "varlen_attn_mixed_res_mmdit.md")
     try:
         text = open(path).read()
     except OSError:
-        return None
+        return {}
     m_d = re.search(r"kernel_digest:\s*([0-9a-f]+)", text)
-    m_t = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", text)
-    if m_d and m_t and m_d.group(1) == digest:
-        return float(m_t.group(1))
-    return None
+    if not m_d or m_d.group(1) != digest:
+        return {}
+    out = {}
+    for key in ("dram_bytes_per_launch", "tensor_pipe_active_pct", "dram_gbs"):
+        m = re.search(key + r":\s*([0-9.eE+]+)", text)
+        if m:
+            out[key] = float(m.group(1))
+    return out
+
+
+def _profiled_traffic(digest: str):
+    return _profiled(digest).get("dram_bytes_per_launch")
 
 
 def rank_seed(rank: int, base: int = 1002) -> int:
@@ -353,7 +362,8 @@ def run_ours(args):
     attn_mean_ms = statistics.mean(attn_ms)
     achieved = flops / (attn_mean_ms * 1e-3) / 1e12
     digest = _kernel_digest()
-    traffic = _profiled_traffic(digest)
+    prof = _profiled(digest)
+    traffic = prof.get("dram_bytes_per_launch")
     result = None
     if rank == 0:
         cpu = None
@@ -381,6 +391,10 @@ def run_ours(args):
                          "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
                          "peak_source": f"{peak_src} bf16 dense (burst)",
                          "launch_ms": attn_mean_ms, "traffic": traffic,
+                         "ncu": {"tensor_pipe_active_pct": prof.get("tensor_pipe_active_pct"),
+                                 "dram_gbs": prof.get("dram_gbs"),
+                                 "source": "profiles/varlen_attn_mixed_res_mmdit.md"}
+                         if prof else None,
                          "kernel_digest": digest},
             "cpu_baseline": cpu,
             "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
