@@ -343,14 +343,17 @@ def run_ours(args):
     value = flops * ws * args.steps / (total_ms * 1e-3) / 1e12
 
     # ---- end to end: host buffers in, host result out ----------------------
-    e2e_mean, h2d, d2h = run_e2e(pv, pw, L, dev, scale, max(3, min(args.steps, 10)),
-                                 out_pad.cpu())
+    # the same job size as the device-timed value: K steps, copies included
+    e2e_mean, h2d, d2h = run_e2e(pv, pw, L, dev, scale, max(3, args.steps), out_pad.cpu())
     e2e_mean = max_over_ranks(e2e_mean, dist, dev)
     e2e_value = flops * ws / (e2e_mean * 1e-3) / 1e12
 
     # ---- block-window variants (Token2Wav), timed per layer ------------------
     bw_meas = measure_block_window(pv, workloads.token2wav(), False, dev, flusher, stream)
     bw32_meas = measure_block_window(pv, workloads.token2wav_f32(), True, dev, flusher, stream)
+    bw_meas["graph"] = measure_block_window_graph(pv, workloads.token2wav(), False, dev, flusher)
+    bw32_meas["graph"] = measure_block_window_graph(pv, workloads.token2wav_f32(), True, dev,
+                                                    flusher)
 
     if pv.get_device_status() != 0:
         raise RuntimeError("device status error during the timed run")
@@ -401,11 +404,13 @@ def run_ours(args):
                     "d2h_bytes_per_step": d2h, "ms_per_step": e2e_mean,
                     "how": "real rows of padded q/k/v from pinned host memory, step, real "
                            "output rows back; copy-in/compute/copy-out on three streams, "
-                           "double-buffered, all steps inside the timed region"},
+                           "double-buffered, all K steps inside the timed region (the first "
+                           "copy-in and the last copy-out included)"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
             "block_window": dict(bw_meas, hbm_frac_own_block_layer=bw_meas["gbs_own_block_layer"]
-                                 / peaks["hbm_gbs"]),
+                                 / peaks["hbm_gbs"],
+                                 hbm_frac_graph=bw_meas["graph"]["gbs"] / peaks["hbm_gbs"]),
             "block_window_f32": dict(bw32_meas,
                                      hbm_frac_own_block_layer=bw32_meas["gbs_own_block_layer"]
                                      / peaks["hbm_gbs"]),
@@ -701,6 +706,47 @@ def measure_block_window(pv, bw, f32, dev, flusher, stream, reps=20):
         "gbs_own_block_layer": nbytes / (per_layer[(0, 0)] * 1e-3) / 1e9,
         "useful_tflops": flops / (total_us * 1e-6) / 1e12,
         "launches": len(bw.layers)}
+
+
+def measure_block_window_graph(pv, bw, f32, dev, flusher, reps=10):
+    """The 22 Token2Wav layers as one CUDA graph, each layer on its own q, k,
+    v and out (22 x the layer's bytes, more than L2), the way the layers run
+    inside the model: no per-launch host gaps or events between layers.  L2
+    is emptied before each replay, outside the events."""
+    fn = pv.block_window_attn_fwd_f32 if f32 else pv.block_window_attn_fwd
+    n_layers = len(bw.layers)
+    qs = [bw.q.to(dev) for _ in range(n_layers)]
+    ks = [bw.k.to(dev) for _ in range(n_layers)]
+    vs = [bw.v.to(dev) for _ in range(n_layers)]
+    outs = [torch.empty_like(qs[0]) for _ in range(n_layers)]
+    side = torch.cuda.Stream(device=dev)
+    side.wait_stream(torch.cuda.current_stream(dev))
+    with torch.cuda.stream(side):
+        for i, (lb, la) in enumerate(bw.layers):   # warm-up outside the capture
+            fn(qs[i], ks[i], vs[i], bw.block, lb, la, out=outs[i])
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        for i, (lb, la) in enumerate(bw.layers):
+            fn(qs[i], ks[i], vs[i], bw.block, lb, la, out=outs[i])
+    torch.cuda.synchronize()
+    stream = torch.cuda.current_stream(dev)
+    ts = []
+    for _ in range(reps):
+        flusher.flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        graph.replay()
+        e1.record(stream)
+        ts.append((e0, e1))
+    torch.cuda.synchronize()
+    us = 1e3 * statistics.median(a.elapsed_time(b) for a, b in ts)
+    nbytes = 4 * qs[0].numel() * qs[0].element_size()
+    return {"us_all_layers": us, "us_per_layer": us / n_layers,
+            "gbs": n_layers * nbytes / (us * 1e-6) / 1e9,
+            "how": f"{n_layers} layers captured in one CUDA graph, each on its own "
+                   f"q/k/v/out ({n_layers * nbytes / 2**20:.0f} MB in all), L2 emptied "
+                   "before each replay"}
 
 
 def run_cfg_combine_only(args, dev):

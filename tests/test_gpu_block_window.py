@@ -74,3 +74,21 @@ def test_window_keys_outside_do_not_matter(pv):
     w2 = workloads.BlockWindowWorkload("p", 1, 96, 2, 64, 24, [(1, 0)], w.q, k2, v2, 6)
     pert = _run(pv, w2, 1, 0)
     assert torch.equal(base[0, :48].view(torch.int16), pert[0, :48].view(torch.int16))
+
+
+def test_graph_replay_matches_eager(pv):
+    # the 22 Token2Wav layers captured in a CUDA graph give the eager launches' bits
+    w = workloads.token2wav(n=480)
+    q, k, v = w.q.cuda(), w.k.cuda(), w.v.cuda()
+    eager = [pv.block_window_attn_fwd(q, k, v, w.block, lb, la) for lb, la in w.layers]
+    outs = [torch.empty_like(q) for _ in w.layers]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        for o, (lb, la) in zip(outs, w.layers):
+            pv.block_window_attn_fwd(q, k, v, w.block, lb, la, out=o)
+    graph.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(eager, outs):
+        assert torch.equal(a.view(torch.int16), b.view(torch.int16))
