@@ -53,11 +53,20 @@ def test_cross_lengths_and_empty_keys(pv, lq, lk):
     _check_full(pv, w, f"Lq={lq} Lk={lk}")
 
 
-def test_many_sequences(pv):
+@pytest.mark.parametrize("D", [64, 128])
+def test_many_sequences(pv, D):
+    # D = 128 with more than 256 sequences runs the 4-slot, 1024-sequence variant
     rng = np.random.default_rng(7)
     L = rng.integers(0, 200, size=300).tolist()
-    w = workloads.random_varlen(L, None, 2, 64, seed=8)
-    _check_full(pv, w, "300 sequences")
+    w = workloads.random_varlen(L, None, 2, D, seed=8)
+    _check_full(pv, w, f"300 sequences D={D}")
+
+
+def test_every_item_single_tile(pv):
+    # no sequence reaches a second 128-row tile: the second MMA issuer only
+    # releases slots and never issues
+    w = workloads.random_varlen([100, 50, 128, 7, 64, 128, 1], None, 3, 128, seed=12)
+    _check_full(pv, w, "single-tile items")
 
 
 def test_max_batch(pv):
