@@ -62,11 +62,21 @@ def _peaks():
     except (OSError, ValueError):
         return dict(FALLBACK_PEAKS), "fallback"
     out = dict(FALLBACK_PEAKS)
+    flat = {}
+
+    def walk(d):   # numbers at any depth, by their own key
+        if isinstance(d, dict):
+            for k, v in d.items():
+                if isinstance(v, (int, float)) and not isinstance(v, bool):
+                    flat.setdefault(k, float(v))
+                else:
+                    walk(v)
+    walk(raw)
 
     def find(keys):
         for k in keys:
-            if k in raw and isinstance(raw[k], (int, float)):
-                return float(raw[k])
+            if k in flat:
+                return flat[k]
         return None
     hbm = find(["hbm_gbs", "hbm_GBps", "hbm_gb_s"])
     bf = find(["bf16_tflops", "bf16_TFLOPs"])
