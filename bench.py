@@ -43,6 +43,8 @@ import workloads  # noqa: E402
 METRIC = "packed varlen attention useful TFLOP/s and % of GB300 bf16 tensor peak"
 UNIT = "TFLOP/s"
 WORKLOAD = "mixed_res_mmdit"
+# FP32 FMA rate of one GB300: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz
+FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 L2_FLUSH_BYTES = 512 << 20
 
@@ -423,7 +425,13 @@ def run_ours(args):
                                  hbm_frac_graph=bw_meas["graph"]["gbs"] / peaks["hbm_gbs"]),
             "block_window_f32": dict(bw32_meas,
                                      hbm_frac_own_block_layer=bw32_meas["gbs_own_block_layer"]
-                                     / peaks["hbm_gbs"]),
+                                     / peaks["hbm_gbs"],
+                                     alu={"bound": "alu", "peak": FP32_PEAK_TFLOPS,
+                                          "unit": "TFLOP/s",
+                                          "achieved_neighbour_layer": bw32_meas["tflops_1_1"],
+                                          "frac": bw32_meas["tflops_1_1"] / FP32_PEAK_TFLOPS,
+                                          "peak_source": "152 SMs x 128 FP32 lanes x 2 FLOP "
+                                                         "x 2.07 GHz"}),
             "cfg_combine": cfg_meas,
             "rope": rope_meas,
             "linear": linear_meas,
@@ -706,7 +714,10 @@ def measure_block_window(pv, bw, f32, dev, flusher, stream, reps=20):
     flops = sum(block_window_flops(bw.n, bw.H, bw.D, bw.block, lb, la) * bw.batch
                 for lb, la in bw.layers)
     n_own = sum(1 for l in bw.layers if l == (0, 0))
+    t11 = block_window_flops(bw.n, bw.H, bw.D, bw.block, 1, 1) * bw.batch / (
+        per_layer[(1, 1)] * 1e-3) / 1e12 if (1, 1) in per_layer else None
     return {
+        "tflops_1_1": t11,
         "workload": f"token2wav {'fp32' if f32 else 'bf16'} batch={bw.batch} n={bw.n} "
                     f"H={bw.H} D={bw.D} block={bw.block}, {n_own} x (0,0) + "
                     f"{len(bw.layers) - n_own} x (1,1) layers",
