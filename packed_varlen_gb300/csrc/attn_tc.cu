@@ -12,17 +12,17 @@
 // twice the tensor-core work of a single-tile item.
 //   warp 0      TMA producer: Q0/Q1 once per item, then K0, V0, K1, V1, ...
 //               through a ring of shared-memory slots.
-//   warp 1      allocates TMEM (S0, S1, O0, O1: 128 columns each); lane 0
+//   warp 1      allocates TMEM (S0, S1, O0, O1: 128 columns each) and
 //               issues tile 0's tcgen05.mma in the order
 //                 S0_0 | PV0_0 S0_1 | PV0_1 S0_2 ...
-//   warp 10     lane 0 issues tile 1's in the same order.
+//   warp 10     issues tile 1's in the same order.
 //               S = Q K^T with both operands in shared memory, fp32 into TMEM;
 //               O += P V with P (bf16) read from TMEM, V from shared memory.
 //               While one tile's softmax runs, the tensor core computes the
-//               other tile's PV and next S.  Two issuing threads keep the
-//               tensor pipe fed: one thread's waits, fences and commits
-//               between 128-wide MMA groups leave the pipe idle about a
-//               third of the time.
+//               other tile's PV and next S.  Each issuer is a whole warp
+//               with one elected lane issuing (warp-uniform operands), and
+//               the two take turns group by group; with two issuers one
+//               thread's waits, fences and commits overlap the other's MMAs.
 //   warps 2..5  softmax of tile 0, one thread per query row (TMEM lane);
 //   warps 6..9  softmax of tile 1.  Each thread reads its row of S, runs the
 //               online softmax in fp32 (exp2 with the scale folded in),
@@ -192,23 +192,31 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ================= TMA producer =================
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_q);
-      tma_prefetch_desc(&tm_k);
-      tma_prefetch_desc(&tm_v);
+    // (warp-wide like the MMA issuers: one elected lane issues the copies)
+    {
+      const bool lead = elect_one();
+      if (lead) {
+        tma_prefetch_desc(&tm_q);
+        tma_prefetch_desc(&tm_k);
+        tma_prefetch_desc(&tm_v);
+      }
       uint32_t q_loads = 0, slot_loads = 0;
       bool ok = true;
+      auto wait_all = [&](uint32_t b, uint32_t parity) -> bool {
+        const bool w = bounded_wait(b, parity, abort_flag, p.status, kWaitLimit);
+        return __all_sync(0xffffffffu, w);
+      };
       auto load_kv = [&](const CUtensorMap *tm, int row, int head) -> bool {
         const uint32_t s = slot_loads % C::kSlots;
         const uint32_t use = slot_loads / C::kSlots;
-        if (!bounded_wait(bar(C::kSlotEmpty + s), (use & 1u) ^ 1u, abort_flag, p.status,
-                          kWaitLimit))
-          return false;
-        mbar_arrive_expect_tx(bar(C::kSlotFull + s), C::kTileBytes);
+        if (!wait_all(bar(C::kSlotEmpty + s), (use & 1u) ^ 1u)) return false;
         const uint32_t dst = sRing + s * C::kTileBytes;
+        if (lead) {
+          mbar_arrive_expect_tx(bar(C::kSlotFull + s), C::kTileBytes);
 #pragma unroll
-        for (int hf = 0; hf < D / 64; ++hf)
-          tma_load_3d(dst + hf * C::kHalfBytes, tm, bar(C::kSlotFull + s), hf * 64, head, row);
+          for (int hf = 0; hf < D / 64; ++hf)
+            tma_load_3d(dst + hf * C::kHalfBytes, tm, bar(C::kSlotFull + s), hf * 64, head, row);
+        }
         ++slot_loads;
         return true;
       };
@@ -216,17 +224,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         const ItemInfo it = item_info(p, order, prefix, i);
         if (it.nk == 0) continue;
         const int ntq = it.rows > kTile ? 2 : 1;
-        if (!bounded_wait(bar(C::kQEmpty), (q_loads & 1u) ^ 1u, abort_flag, p.status,
-                          kWaitLimit)) {
+        if (!wait_all(bar(C::kQEmpty), (q_loads & 1u) ^ 1u)) {
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(bar(C::kQFull), ntq * C::kTileBytes);
-        for (int t = 0; t < ntq; ++t) {
+        if (lead) {
+          mbar_arrive_expect_tx(bar(C::kQFull), ntq * C::kTileBytes);
+          for (int t = 0; t < ntq; ++t) {
 #pragma unroll
-          for (int hf = 0; hf < D / 64; ++hf)
-            tma_load_3d(sQ + t * C::kTileBytes + hf * C::kHalfBytes, &tm_q, bar(C::kQFull),
-                        hf * 64, it.head, it.q_row0 + t * kTile);
+            for (int hf = 0; hf < D / 64; ++hf)
+              tma_load_3d(sQ + t * C::kTileBytes + hf * C::kHalfBytes, &tm_q, bar(C::kQFull),
+                          hf * 64, it.head, it.q_row0 + t * kTile);
+          }
         }
         ++q_loads;
         for (int j = 0; j < it.nk && ok; ++j) {
@@ -251,15 +260,23 @@ __global__ void __launch_bounds__(kThreads, 1)
     // slot (or the Q buffer) with one arrival on a two-arrival barrier: a
     // commit once its MMAs reading the slot are done, or a plain arrive when
     // its tile is absent from the item.
+    // The whole warp runs the issuer, so every operand of an MMA is
+    // warp-uniform, and one elected lane issues each MMA, commit and
+    // arrive: tcgen05.mma issued from a lone lane's control flow costs about
+    // 100 cycles per instruction, against 64 of tensor work for these shapes.
     const int t = warp == 1 ? 0 : 1;
-    if (lane == 0) {
+    {
+      const bool lead = elect_one();
       uint32_t q_uses = 0, slot_uses = 0, issued = 0, p_waits = 0;
       bool ok = true;
+      auto wait_all = [&](uint32_t b, uint32_t parity) -> bool {
+        const bool w = bounded_wait(b, parity, abort_flag, p.status, kWaitLimit);
+        return __all_sync(0xffffffffu, w);
+      };
       // next ring slot in consumption order, once its load has landed
       auto wait_slot = [&](uint32_t &s) -> bool {
         s = slot_uses % C::kSlots;
-        return bounded_wait(bar(C::kSlotFull + s), (slot_uses / C::kSlots) & 1u, abort_flag,
-                            p.status, kWaitLimit);
+        return wait_all(bar(C::kSlotFull + s), (slot_uses / C::kSlots) & 1u);
       };
       // S_t = Q_t K^T into S buffer t (Q/K K-major, SBO = 8 rows x 128 B)
       // (descriptors advance by adding the byte offset >> 4 to the start
@@ -273,7 +290,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = ((kk >> 2) * C::kHalfBytes + (kk & 3) * 32) >> 4;
-          mma_ss(d_s, qdesc0 + off, b0 + off, C::kIdescS, kk > 0 ? 1u : 0u);
+          if (lead) mma_ss(d_s, qdesc0 + off, b0 + off, C::kIdescS, kk > 0 ? 1u : 0u);
         }
       };
       // O_t += P_t V (P_t is in the first 64 columns of the S buffer)
@@ -281,8 +298,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint64_t b0 = vdesc0 + ((slot * C::kTileBytes) >> 4);
 #pragma unroll
         for (int kk = 0; kk < kTile / 16; ++kk) {
-          mma_ts(d_o, d_s + kk * 8, b0 + ((kk * 16 * 128) >> 4), C::kIdescO,
-                 (first && kk == 0) ? 0u : 1u);
+          if (lead)
+            mma_ts(d_o, d_s + kk * 8, b0 + ((kk * 16 * 128) >> 4), C::kIdescO,
+                   (first && kk == 0) ? 0u : 1u);
         }
       };
       // The two issuers take turns group by group (S0_0, S1_0, [PV0_0 S0_1],
@@ -292,11 +310,11 @@ __global__ void __launch_bounds__(kThreads, 1)
       uint32_t turns = 0;
       auto take_turn = [&]() -> bool {
         const uint32_t parity = t == 0 ? ((turns & 1u) ^ 1u) : (turns & 1u);
-        return bounded_wait(bar(C::kTurn + t), parity, abort_flag, p.status, kWaitLimit);
+        return wait_all(bar(C::kTurn + t), parity);
       };
       auto pass_turn = [&]() {
         ++turns;
-        mbar_arrive(bar(C::kTurn + (1 - t)));
+        if (lead) mbar_arrive(bar(C::kTurn + (1 - t)));
       };
       for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x) {
         const ItemInfo it = item_info(p, order, prefix, i);
@@ -304,12 +322,13 @@ __global__ void __launch_bounds__(kThreads, 1)
         const bool mine = it.rows > t * kTile;   // this issuer's tile is in the item
         // release a slot / the Q buffer: after this tile's MMAs, or at once
         auto release = [&](uint32_t b) {
+          if (!lead) return;
           if (mine)
             mma_commit(b);
           else
             mbar_arrive(b);
         };
-        if (!bounded_wait(bar(C::kQFull), q_uses & 1u, abort_flag, p.status, kWaitLimit)) {
+        if (!wait_all(bar(C::kQFull), q_uses & 1u)) {
           ok = false;
           break;
         }
@@ -325,7 +344,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           issued = 1;
         }
         pass_turn();
-        if (mine) mma_commit(bar(C::kSFull + t));
+        if (mine && lead) mma_commit(bar(C::kSFull + t));
         release(bar(C::kSlotEmpty + sk));
         ++slot_uses;
         if (it.nk == 1) release(bar(C::kQEmpty));
@@ -341,19 +360,19 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = false;
             break;
           }
-          // P_j written by this tile's softmax
+          // the issue turn first (the order is fixed, so holding it early
+          // blocks nobody), then P_j written by this tile's softmax
+          if (!take_turn()) {
+            ok = false;
+            break;
+          }
           if (mine) {
-            if (!bounded_wait(bar(C::kPReady + t), p_waits & 1u, abort_flag, p.status,
-                              kWaitLimit)) {
+            if (!wait_all(bar(C::kPReady + t), p_waits & 1u)) {
               ok = false;
               break;
             }
             ++p_waits;
             fence_after_sync();
-          }
-          if (!take_turn()) {
-            ok = false;
-            break;
           }
           // PV_j, then S_{j+1} (after the PV that reads P from the S buffer)
           if (mine) {
@@ -361,7 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (more) issue_s(sk2);
           }
           pass_turn();
-          if (mine) {
+          if (mine && lead) {
             if (more)
               mma_commit(bar(C::kSFull + t));
             else
@@ -377,7 +396,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       // every MMA this thread issued has finished before TMEM is released
       if (issued) {
-        mma_commit(bar(C::kFinal + t));
+        if (lead) mma_commit(bar(C::kFinal + t));
         drain_wait(bar(C::kFinal + t), 0, kWaitLimit);
       }
     }

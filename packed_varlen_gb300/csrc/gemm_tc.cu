@@ -25,7 +25,9 @@
 // both CTAs once its MMAs are done (a slot holds the peer's w half too);
 // warps 2-5 drain a finished accumulator (each warp its TMEM lane quadrant),
 // add the bias, round to bf16 and store, while the MMA warp fills the other
-// accumulator.  Tile pairs go round-robin over the clusters, N-block fastest,
+// accumulator.  Warps 0 and 1 run their loops warp-wide and one elected
+// lane issues each copy, MMA and commit, so MMA operands are warp-uniform.
+// Tile pairs go round-robin over the clusters, N-block fastest,
 // so a wave shares x rows and w stays in L2.  Every wait is bounded; a
 // timeout records PA_DEVICE_ERR_TIMEOUT.
 #include <cuda_bf16.h>
@@ -116,9 +118,13 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
 
   if (warp == 0) {
     // ================= TMA producer =================
-    if (lane == 0) {
-      tma_prefetch_desc(&tm_x);
-      tma_prefetch_desc(&tm_w);
+    // (warp-wide like the issuer: one elected lane issues the copies)
+    {
+      const bool lead = elect_one();
+      if (lead) {
+        tma_prefetch_desc(&tm_x);
+        tma_prefetch_desc(&tm_w);
+      }
       uint32_t loads = 0;
       bool ok = true;
       for (int tp = cl; tp < p.n_pairs && ok; tp += n_cl) {
@@ -126,17 +132,20 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
         const int n0 = (tp % p.tiles_n) * kBN + rank * (kBN / kCluster);
         for (int kb = 0; kb < p.k_blocks; ++kb) {
           const uint32_t s = loads % kStages, use = loads / kStages;
-          if (!bounded_wait(bar(C::kEmpty + s), (use & 1u) ^ 1u, abort_flag, p.status,
-                            kWaitLimit)) {
+          const bool w = bounded_wait(bar(C::kEmpty + s), (use & 1u) ^ 1u, abort_flag, p.status,
+                                      kWaitLimit);
+          if (!__all_sync(0xffffffffu, w)) {
             ok = false;
             break;
           }
-          mbar_arrive_expect_tx(bar(C::kFull + s), C::kStageBytes);
           const uint32_t dst = base + s * C::kStageBytes;
-          tma_load_2d(dst, &tm_x, bar(C::kFull + s), kb * kBK, m0);
-          // this CTA's half of the w tile, into both CTAs of the pair
-          tma_load_2d_multicast(dst + C::kABytes + rank * (C::kBBytes / kCluster), &tm_w,
-                                bar(C::kFull + s), kb * kBK, n0, kPairMask);
+          if (lead) {
+            mbar_arrive_expect_tx(bar(C::kFull + s), C::kStageBytes);
+            tma_load_2d(dst, &tm_x, bar(C::kFull + s), kb * kBK, m0);
+            // this CTA's half of the w tile, into both CTAs of the pair
+            tma_load_2d_multicast(dst + C::kABytes + rank * (C::kBBytes / kCluster), &tm_w,
+                                  bar(C::kFull + s), kb * kBK, n0, kPairMask);
+          }
           ++loads;
         }
       }
@@ -150,7 +159,16 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     }
   } else if (warp == 1) {
     // ================= MMA issuer =================
-    if (lane == 0) {
+    // The whole warp runs the issuer, so every operand of an MMA is
+    // warp-uniform, and one elected lane issues each MMA and commit:
+    // tcgen05.mma issued from a lone lane's control flow pays a large
+    // per-instruction cost.
+    {
+      const bool lead = elect_one();
+      auto wait_all = [&](uint32_t b, uint32_t parity) -> bool {
+        const bool w = bounded_wait(b, parity, abort_flag, p.status, kWaitLimit);
+        return __all_sync(0xffffffffu, w);
+      };
       uint32_t uses = 0, tiles_done = 0;
       bool ok = true, issued = false;
       // descriptors advance by adding the byte offset >> 4 to the start
@@ -159,8 +177,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
       const uint64_t bdesc0 = sdesc_sw128(base + C::kABytes, 16, 1024);
       for (int tp = cl; tp < p.n_pairs && ok; tp += n_cl, ++tiles_done) {
         const uint32_t buf = tiles_done & 1u, buse = tiles_done >> 1;
-        if (!bounded_wait(bar(C::kAccEmpty + buf), (buse & 1u) ^ 1u, abort_flag, p.status,
-                          kWaitLimit)) {
+        if (!wait_all(bar(C::kAccEmpty + buf), (buse & 1u) ^ 1u)) {
           ok = false;
           break;
         }
@@ -170,8 +187,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t s = uses % kStages;
           // the TMA bytes completed on this barrier are visible to the MMA
           // once the wait returns (no TMEM hand-off, so no tcgen05 fence)
-          if (!bounded_wait(bar(C::kFull + s), (uses / kStages) & 1u, abort_flag, p.status,
-                            kWaitLimit)) {
+          if (!wait_all(bar(C::kFull + s), (uses / kStages) & 1u)) {
             ok = false;
             break;
           }
@@ -179,19 +195,20 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
           const uint64_t b = bdesc0 + ((s * C::kStageBytes) >> 4);
 #pragma unroll
           for (int kk = 0; kk < kBK / 16; ++kk)
-            mma_ss(d, a + ((kk * 32) >> 4), b + ((kk * 32) >> 4), C::kIdesc,
-                   (kb > 0 || kk > 0) ? 1u : 0u);
+            if (lead)
+              mma_ss(d, a + ((kk * 32) >> 4), b + ((kk * 32) >> 4), C::kIdesc,
+                     (kb > 0 || kk > 0) ? 1u : 0u);
           issued = true;
           // the slot (with the peer's w half) is free once both CTAs' MMAs finish
-          mma_commit_multicast(bar(C::kEmpty + s), kPairMask);
+          if (lead) mma_commit_multicast(bar(C::kEmpty + s), kPairMask);
           ++uses;
         }
         if (!ok) break;
-        mma_commit(bar(C::kAccFull + buf));
+        if (lead) mma_commit(bar(C::kAccFull + buf));
       }
       // every MMA issued so far has finished before TMEM is released
       if (issued) {
-        mma_commit(bar(C::kFinal));
+        if (lead) mma_commit(bar(C::kFinal));
         drain_wait(bar(C::kFinal), 0, kWaitLimit);
       }
     }
