@@ -104,7 +104,11 @@ __global__ void __launch_bounds__(kScanThreads)
 }
 
 // ---------------------------------------------------------------------------
-// pack / unpack: one padded row per loop step of a CTA, 16-byte vectors.
+// pack / unpack.  The work is split into chunks of `rows_per_chunk` rows of
+// one sequence (chunk c: sequence c / chunks_per_seq); a chunk's rows are
+// contiguous in both layouts, so one warp copies it as one run of 16-byte
+// vectors with four loads in flight per lane.  Warps stride over all chunks
+// of all sequences, so a long sequence is spread over the whole GPU.
 // ---------------------------------------------------------------------------
 constexpr int kCopyThreads = 256;
 
@@ -112,22 +116,40 @@ template <bool kPack>
 __global__ void __launch_bounds__(kCopyThreads)
     repack_kernel(const uint4 *__restrict__ src, uint4 *__restrict__ dst,
                   const int32_t *__restrict__ cu, int batch, int s_max, int total,
-                  int64_t row_vecs, int32_t *status) {
-  const int b = blockIdx.y;
-  const int c0 = __ldg(cu + b), c1 = __ldg(cu + b + 1);
-  const bool ok = c0 >= 0 && c0 <= c1 && c1 <= total && (b > 0 || c0 == 0);
-  if (!ok || c1 - c0 > s_max) {
-    if (blockIdx.x == 0 && threadIdx.x == 0)
-      record_error(status, ok ? PA_DEVICE_ERR_MAX_LEN : PA_DEVICE_ERR_CU_SEQLENS);
-    return;
-  }
-  const int L = c1 - c0;
-  for (int r = blockIdx.x; r < L; r += gridDim.x) {
-    const int64_t padded_row = static_cast<int64_t>(b) * s_max + r;
-    const int64_t flat_row = static_cast<int64_t>(c0) + r;
+                  int64_t row_vecs, int rows_per_chunk, int32_t *status) {
+  const int lane = threadIdx.x & 31;
+  const int64_t chunks_per_seq = (s_max + rows_per_chunk - 1) / rows_per_chunk;
+  const int64_t n_chunks = chunks_per_seq * batch;
+  const int64_t n_warps = static_cast<int64_t>(gridDim.x) * (kCopyThreads / 32);
+  for (int64_t c = (static_cast<int64_t>(blockIdx.x) * kCopyThreads + threadIdx.x) >> 5;
+       c < n_chunks; c += n_warps) {
+    const int b = static_cast<int>(c / chunks_per_seq);
+    const int64_t r0 = (c - static_cast<int64_t>(b) * chunks_per_seq) * rows_per_chunk;
+    const int c0 = __ldg(cu + b), c1 = __ldg(cu + b + 1);
+    const bool ok = c0 >= 0 && c0 <= c1 && c1 <= total && (b > 0 || c0 == 0);
+    if (!ok || c1 - c0 > s_max) {
+      if (r0 == 0 && lane == 0)
+        record_error(status, ok ? PA_DEVICE_ERR_MAX_LEN : PA_DEVICE_ERR_CU_SEQLENS);
+      continue;
+    }
+    const int64_t L = c1 - c0;
+    if (r0 >= L) continue;
+    const int64_t rows = L - r0 < rows_per_chunk ? L - r0 : rows_per_chunk;
+    const int64_t padded_row = static_cast<int64_t>(b) * s_max + r0;
+    const int64_t flat_row = static_cast<int64_t>(c0) + r0;
     const uint4 *s = src + (kPack ? padded_row : flat_row) * row_vecs;
     uint4 *d = dst + (kPack ? flat_row : padded_row) * row_vecs;
-    for (int64_t i = threadIdx.x; i < row_vecs; i += kCopyThreads) d[i] = __ldg(s + i);
+    const int64_t n = rows * row_vecs;
+    int64_t i = lane;
+    for (; i + 96 < n; i += 128) {
+      const uint4 v0 = __ldg(s + i), v1 = __ldg(s + i + 32), v2 = __ldg(s + i + 64),
+                  v3 = __ldg(s + i + 96);
+      d[i] = v0;
+      d[i + 32] = v1;
+      d[i + 64] = v2;
+      d[i + 96] = v3;
+    }
+    for (; i < n; i += 32) d[i] = __ldg(s + i);
   }
 }
 
@@ -269,21 +291,24 @@ static pa_status repack(bool is_pack, const void *src, void *dst, const int32_t 
   int32_t *status;
   int sms;
   if (device_context(&status, &sms) != cudaSuccess) return PA_ERR_CUDA;
-  // enough CTAs to cover the GPU several times; each strides over its rows
-  int per_seq = (sms * 8 + batch - 1) / batch;
-  if (per_seq > s_max) per_seq = s_max;
-  if (per_seq < 1) per_seq = 1;
-  dim3 grid(per_seq, batch);
+  // chunks of about 16 KB; a grid that fills every SM eight CTAs deep
   const int64_t vecs = row_bytes / 16;
+  int64_t rows_per_chunk = 16384 / row_bytes;
+  if (rows_per_chunk < 1) rows_per_chunk = 1;
+  if (rows_per_chunk > s_max) rows_per_chunk = s_max;
+  const int64_t n_chunks = static_cast<int64_t>(batch) * ((s_max + rows_per_chunk - 1) / rows_per_chunk);
+  int64_t grid = (n_chunks + kCopyThreads / 32 - 1) / (kCopyThreads / 32);
+  if (grid > static_cast<int64_t>(sms) * 8) grid = static_cast<int64_t>(sms) * 8;
   auto st = reinterpret_cast<cudaStream_t>(stream);
+  const int rpc = static_cast<int>(rows_per_chunk);
   if (is_pack)
-    repack_kernel<true><<<grid, kCopyThreads, 0, st>>>(static_cast<const uint4 *>(src),
-                                                        static_cast<uint4 *>(dst), cu, batch,
-                                                        s_max, total, vecs, status);
+    repack_kernel<true><<<static_cast<unsigned>(grid), kCopyThreads, 0, st>>>(
+        static_cast<const uint4 *>(src), static_cast<uint4 *>(dst), cu, batch, s_max, total,
+        vecs, rpc, status);
   else
-    repack_kernel<false><<<grid, kCopyThreads, 0, st>>>(static_cast<const uint4 *>(src),
-                                                         static_cast<uint4 *>(dst), cu, batch,
-                                                         s_max, total, vecs, status);
+    repack_kernel<false><<<static_cast<unsigned>(grid), kCopyThreads, 0, st>>>(
+        static_cast<const uint4 *>(src), static_cast<uint4 *>(dst), cu, batch, s_max, total,
+        vecs, rpc, status);
   return from_cuda(cudaGetLastError());
 }
 

@@ -64,6 +64,36 @@ def test_pack_full_mixed_res(pv):
     assert np.array_equal(_i16(flat), oracle.pack(_i16(pw.k), pw.lengths))
 
 
+@pytest.mark.parametrize("lengths,H,D", [
+    (np.random.default_rng(3).integers(0, 300, 200).tolist(), 2, 64),   # many sequences
+    ([3, 1, 2], 24, 512),                                              # 24 KB rows: one per chunk
+])
+def test_pack_unpack_chunking(pv, lengths, H, D):
+    # the copy is split into chunks of ~16 KB of one sequence's rows; every
+    # sequence, chunk tail and row size must land exactly
+    pw = workloads.padded(lengths, H, D, seed=len(lengths))
+    cu = pv.cu_seqlens_from_lengths(torch.tensor(lengths, dtype=torch.int32, device="cuda"))
+    T = sum(lengths)
+    flat = pv.pack(pw.q.cuda(), cu, T)
+    want = oracle.pack(_i16(pw.q), lengths)
+    assert np.array_equal(_i16(flat), want)
+    target = torch.full_like(pw.q, 3.0).cuda()
+    pv.unpack(flat, cu, target)
+    assert np.array_equal(_i16(target), oracle.unpack(want, lengths, _i16(torch.full_like(pw.q, 3.0))))
+    assert pv.get_device_status() == 0
+
+
+def test_pack_skips_only_the_bad_sequence(pv):
+    # sequence 1 ends past `total`: it is skipped and reported, sequence 0 is copied
+    padded = torch.arange(2 * 8 * 8, dtype=torch.float32).to(torch.bfloat16).view(2, 8, 8).cuda()
+    cu = torch.tensor([0, 3, 9], dtype=torch.int32, device="cuda")
+    flat = torch.full((7, 8), -1.0, dtype=torch.bfloat16, device="cuda")
+    pv.pack(padded, cu, 7, out=flat)
+    assert pv.get_device_status() == 1   # PA_DEVICE_ERR_CU_SEQLENS
+    assert torch.equal(flat[:3].cpu(), padded[0, :3].cpu())
+    assert (flat[3:].float() == -1.0).all()
+
+
 def test_pack_rejects_long_sequence(pv):
     padded = torch.zeros(2, 4, 8, dtype=torch.bfloat16, device="cuda")
     cu = torch.tensor([0, 5, 7], dtype=torch.int32, device="cuda")   # 5 > s_max = 4
