@@ -81,8 +81,14 @@ typedef enum {
  *       (rows >= cu_seqlens_q[batch] are left untouched)
  * cu_seqlens_q / cu_seqlens_k: device int32 [batch + 1]
  * batch in [1, PA_MAX_BATCH]; total_q/total_k >= cu[batch] (extra rows are
- * padding that is neither read as keys nor written); max_q / max_k bound every
- * sequence length; H >= 1; D in {64, 128}; scale finite (1/sqrt(D) is usual).
+ * padding that belongs to no sequence and is never written); max_q / max_k
+ * bound every sequence length; H >= 1; D in {64, 128}; scale finite
+ * (1/sqrt(D) is usual).
+ * Rows outside a sequence never change its result, whatever their bits
+ * (NaN and Inf included): the last 128-row key tile of a sequence is loaded
+ * whole, so up to 127 rows after the sequence end (the next sequence's rows
+ * or trailing padding, within total_k) are read into shared memory, but
+ * their scores are masked and their value rows are cleared before use.
  * q, k, v, out must be 16-byte aligned.
  * Deterministic: every output row is computed by one CTA in a fixed order, so
  * a sequence's result does not depend on which other sequences share the

@@ -135,6 +135,24 @@ __device__ __forceinline__ ItemInfo item_info(const TcParams &p, const int32_t *
   return it;
 }
 
+// Whole warp: zero key rows [valid, 128) of a V tile in shared memory.  The
+// tile is D / 64 column halves of 128 rows x 128 bytes; the 128-byte swizzle
+// only permutes the 16-byte chunks inside a row, so a whole row is cleared
+// without unswizzling.  The fences order the stores after the TMA bytes that
+// landed and before the tensor core's reads (both are async-proxy accesses).
+template <int D>
+__device__ __forceinline__ void zero_v_tail(uint8_t *tile, int valid, int lane) {
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+  const int per_half = (kTile - valid) * 8;   // 16-byte chunks per half
+  for (int c = lane; c < per_half * (D / 64); c += 32) {
+    const int hf = c / per_half, r = c - hf * per_half;
+    *reinterpret_cast<uint4 *>(tile + hf * (kTile * 128) + (valid + (r >> 3)) * 128 +
+                               (r & 7) * 16) = make_uint4(0u, 0u, 0u, 0u);
+  }
+  asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+  __syncwarp();
+}
+
 template <int D, int kSlots, int kMaxSeqs>
 __global__ void __launch_bounds__(kThreads, 1)
     varlen_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
@@ -356,6 +374,17 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           ++slot_uses;
+          // The last key tile of a sequence whose length is not a multiple
+          // of 128 holds rows past the sequence end (the next sequence's, or
+          // the buffer's trailing rows).  P is 0 there, but 0 * Inf and
+          // 0 * NaN are NaN, so those V rows are zeroed before any PV reads
+          // the slot.  Tile 0's issuer runs for every item and issues its PV
+          // before tile 1's (the turn order), so it alone clears the rows.
+          if (t == 0 && key_tile(it, j) == it.nk - 1) {
+            const int valid = it.lk - (it.nk - 1) * kTile;
+            if (valid < kTile)
+              zero_v_tail<D>(gbase + C::kRingOff + sv * C::kTileBytes, valid, lane);
+          }
           if (more && !wait_slot(sk2)) {
             ok = false;
             break;

@@ -46,3 +46,34 @@ def sample_rows(lengths, per_seq=12, seed=0, tile=128):
             rows += [start + r for r in sorted(cand)]
         start += L
     return np.array(rows, dtype=np.int64)
+
+
+def item_rows(lengths, item=256, tile=128, seed=0):
+    """One random query row from every 128-row tile of every sequence (so
+    both tiles of every 256-row work item of the varlen kernel), plus each
+    sequence's first and last rows and the rows on either side of every tile
+    edge that a sequence's last tile creates.  The oracle computes all heads
+    of a row, so every (sequence, head, work item) is checked."""
+    rng = np.random.default_rng(seed)
+    rows, start = [], 0
+    for L in lengths:
+        if L > 0:
+            cand = {0, L - 1, (L - 1) // tile * tile, max(0, (L - 1) // tile * tile - 1)}
+            for t0 in range(0, L, tile):
+                cand.add(int(rng.integers(t0, min(L, t0 + tile))))
+            rows += [start + r for r in sorted(cand)]
+        start += L
+    return np.array(rows, dtype=np.int64)
+
+
+def items_covered(rows, lengths, item=256, tile=128):
+    """Per sequence, the sets of (item, tile) indices the given global rows
+    fall in, and the full sets they should cover."""
+    got, want, start = [], [], 0
+    rows = np.asarray(rows)
+    for L in lengths:
+        local = rows[(rows >= start) & (rows < start + L)] - start
+        got.append({(int(r) // item, (int(r) % item) // tile) for r in local})
+        want.append({(t // item, (t % item) // tile) for t in range(0, L, tile)})
+        start += L
+    return got, want

@@ -6,7 +6,7 @@ import torch
 
 import oracle
 import workloads
-from helpers import assert_close_to_oracle, gpu_varlen, sample_rows
+from helpers import assert_close_to_oracle, gpu_varlen, item_rows, items_covered, sample_rows
 
 pytestmark = pytest.mark.gpu
 
@@ -86,10 +86,15 @@ def test_scale_argument(pv):
 
 @pytest.mark.slow
 @pytest.mark.parametrize("name", ["mixed_res_mmdit", "single_edit", "cfg_dynamic_batch"])
-def test_full_size_configs_sampled(pv, name):
+def test_full_size_configs_every_item(pv, name):
+    # one query row of every 128-row tile of every sequence, all heads: every
+    # (sequence, head, 256-row work item) the scheduler hands out, and both
+    # of its tiles, is compared with the oracle
     w = workloads.VARLEN_CONFIGS[name]()
     out, cu_q, _ = gpu_varlen(pv, w)
-    rows = sample_rows(w.lengths_q, per_seq=8, seed=1)
+    rows = item_rows(w.lengths_q, seed=1)
+    got_items, want_items = items_covered(rows, w.lengths_q)
+    assert got_items == want_items
     cu = oracle.cu_seqlens_from_lengths(w.lengths_q)
     want = oracle.varlen_attention(w.q, w.k, w.v, cu, cu, w.scale, rows=rows)
     assert_close_to_oracle(oracle.to_f64(out[rows]), want, name)
@@ -169,3 +174,63 @@ def test_device_checks_record_errors(pv):
     assert (out[:40].float() == 3.0).all()
     assert (out[40:].float() != 3.0).any()
     assert pv.get_device_status() == 0      # cleared by the read
+
+
+def _poison(t: torch.Tensor, rows: slice) -> torch.Tensor:
+    """Copy of t whose given rows hold NaN, +Inf and -Inf in turn (element by
+    element), so no finite factor can cancel them."""
+    bad = t.clone()
+    block = bad[rows]
+    vals = torch.tensor([float("nan"), float("inf"), float("-inf")], dtype=t.dtype)
+    flat = vals.repeat(block.numel() // 3 + 1)[:block.numel()].view(block.shape)
+    bad[rows] = flat
+    return bad
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_nonfinite_padded_tail(pv, D):
+    # The auto-padded tail of "[Perf][qwen-image-edit] Skip attention-mask to
+    # avoid varlen path" (Test Result: a 1328x1328 image, 6889 tokens padded
+    # to 6896).  6889 = 53 * 128 + 105, so the last key tile loads the 7 pad
+    # rows; filled with NaN / +-Inf they must contribute nothing.
+    L, T = 6889, 6896
+    base = workloads.random_varlen([T], None, 2, D, seed=6889 + D)
+    fin = workloads.VarlenWorkload("tail", [L], [L], 2, D, base.q, base.k, base.v, 0, pad_rows=7)
+    bad = workloads.VarlenWorkload("tail_nonfinite", [L], [L], 2, D,
+                                   _poison(base.q, slice(L, T)), _poison(base.k, slice(L, T)),
+                                   _poison(base.v, slice(L, T)), 0, pad_rows=7)
+    got_fin, _, _ = gpu_varlen(pv, fin)
+    got_bad, _, _ = gpu_varlen(pv, bad)
+    assert torch.isnan(got_bad[L:].float()).all(), "pad rows were written"
+    assert torch.equal(got_bad[:L].view(torch.int16), got_fin[:L].view(torch.int16)), \
+        "non-finite pad rows changed the valid rows"
+    # key-padding-masked dense attention over the finite buffer
+    want = oracle.key_padding_attention(base.q, base.k, base.v, L, fin.scale,
+                                        rows=np.arange(L))
+    assert_close_to_oracle(oracle.to_f64(got_bad[:L]), want, f"6889->6896 tail D={D}")
+    assert pv.get_device_status() == 0
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("lengths", [[300, 200], [129, 1000, 44]])
+def test_nonfinite_neighbour_rows_do_not_leak(pv, D, lengths):
+    # The first 127 key/value rows of sequence 1 (and the query rows) are
+    # non-finite; sequence 0's last key tile spans some of them.  Sequence 0
+    # must still match the oracle and equal its run alone bit for bit.
+    w = workloads.random_varlen(lengths, None, 3, D, seed=41 + D)
+    s1 = slice(lengths[0], lengths[0] + min(127, lengths[1]))
+    bad = workloads.VarlenWorkload("neighbour_nonfinite", w.lengths_q, w.lengths_k, w.H, w.D,
+                                   _poison(w.q, s1), _poison(w.k, s1), _poison(w.v, s1), w.seed)
+    packed, _, _ = gpu_varlen(pv, bad)
+    L0 = lengths[0]
+    alone = _alone(pv, w, 0)
+    assert torch.equal(packed[:L0].view(torch.int16), alone.view(torch.int16))
+    cu = oracle.cu_seqlens_from_lengths(lengths)
+    want = oracle.varlen_attention(w.q, w.k, w.v, cu, cu, w.scale, rows=np.arange(L0))
+    assert_close_to_oracle(oracle.to_f64(packed[:L0]), want, f"sequence 0 of {lengths}")
+    if len(lengths) > 2:   # a sequence after the poisoned one is unaffected too
+        s2 = sum(lengths[:2])
+        want2 = oracle.varlen_attention(w.q, w.k, w.v, cu, cu, w.scale,
+                                        rows=np.arange(s2, s2 + lengths[2]))
+        assert_close_to_oracle(oracle.to_f64(packed[s2:s2 + lengths[2]]), want2, "sequence 2")
+    assert pv.get_device_status() == 0
