@@ -1,5 +1,5 @@
 // Thin inline-PTX wrappers for the sm_100-family asynchronous machinery used by
-// the attention kernels: mbarriers with bounded waits, TMA tensor loads,
+// the tensor-core kernels: mbarriers with bounded waits, TMA tensor loads,
 // tcgen05 MMA / commit / TMEM load-store / allocation and the shared-memory
 // and instruction descriptors.  Written from the PTX ISA descriptions of these
 // instructions; every wait is bounded (see bounded_wait).
@@ -95,16 +95,16 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap *map
       : "memory");
 }
 
-// 2-D tiled load multicast to the CTAs of the cluster in `mask`: the tile
-// lands at offset `dst` of each destination CTA's shared memory and completes
-// bytes on the mbarrier at offset `bar` of each.
-__device__ __forceinline__ void tma_load_2d_multicast(uint32_t dst, const CUtensorMap *map,
-                                                      uint32_t bar, int c0, int c1,
-                                                      uint16_t mask) {
+// 2-D tiled load into this CTA's shared memory whose completed bytes are
+// counted on an mbarrier of either CTA of a cta_group::2 pair: `bar` is a
+// shared::cluster address (see mapa_shared), so both CTAs of the pair can
+// report their bytes to the one barrier that the MMA-issuing CTA waits on.
+__device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap *map,
+                                                 uint32_t bar, int c0, int c1) {
   asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;\n" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "h"(mask)
+      "cp.async.bulk.tensor.2d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%3, %4}], [%2];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1)
       : "memory");
 }
 
@@ -118,6 +118,33 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
 __device__ __forceinline__ void cluster_sync() {
   asm volatile("barrier.cluster.arrive.release.aligned;\n" ::: "memory");
   asm volatile("barrier.cluster.wait.acquire.aligned;\n" ::: "memory");
+}
+
+// shared::cluster address of the object at shared::cta address `addr` in the
+// cluster's CTA `rank`.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t addr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;\n" : "=r"(r) : "r"(addr), "r"(rank));
+  return r;
+}
+// One arrival on an mbarrier of any CTA of the cluster (shared::cluster
+// address), ordered after this thread's earlier memory accesses at cluster
+// scope.
+__device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(bar_cluster)
+               : "memory");
+}
+// try_wait with cluster-scope acquire: for barriers that other CTAs arrive on.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
 }
 
 // ---------------------------------------------------------------- tcgen05
@@ -144,15 +171,6 @@ __device__ __forceinline__ void mma_commit(uint32_t bar) {
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
       : "memory");
 }
-// Arrive on the mbarrier at offset `bar` of every CTA in `mask` once every
-// tcgen05 op issued so far by this thread is done.
-__device__ __forceinline__ void mma_commit_multicast(uint32_t bar, uint16_t mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;\n" ::"r"(bar),
-      "h"(mask)
-      : "memory");
-}
 // D[tmem] (+)= A[smem] * B[smem]
 __device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
                                        uint32_t idesc, uint32_t accumulate) {
@@ -170,6 +188,40 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
       "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+
+// ---- cta_group::2: two CTAs of a cluster (ranks 2i, 2i + 1) share one MMA.
+// A kernel uses one cta_group for all of its tcgen05 instructions.  The
+// allocation is collective: one warp of EACH CTA of the pair executes it,
+// and both receive the same TMEM address.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;\n" ::"r"(dst),
+               "r"(ncols)
+               : "memory");
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;\n" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;\n" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+// Arrive on the mbarrier at shared::cluster address `bar` (either CTA of
+// the pair) once every tcgen05 op issued so far by this thread is done.
+__device__ __forceinline__ void mma_commit_pair(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.b64 [%0];\n" ::"r"(bar)
+      : "memory");
+}
+// Issued by one thread of the even CTA: D (M = 256 rows, rows 0-127 in the
+// even CTA's TMEM, 128-255 in the odd CTA's) (+)= A * B, where each CTA
+// holds its 128 rows of A and its half of B's N columns at the same
+// shared-memory offsets the descriptors name.
+__device__ __forceinline__ void mma_ss_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
 // Instruction descriptor of kind::f16: bf16 A and B, fp32 D, dense.

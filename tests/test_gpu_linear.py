@@ -65,10 +65,11 @@ def test_packed_equals_per_request_bitwise(pv):
 
 
 def test_row_offset_does_not_change_bits(pv):
-    # the same rows at every offset within a 128-row tile give the same bits
+    # the same rows at every offset within a 256-row pair tile give the same
+    # bits (a shift of 128 moves a row from one CTA of the pair to the other)
     w = workloads.linear_case([400], 512, 256, seed=8)
     base = _run(pv, w.x, w.w, w.bias)
-    for shift in (1, 5, 64, 127, 128):
+    for shift in (1, 5, 64, 127, 128, 200, 255, 256):
         moved = _run(pv, w.x[shift:].contiguous(), w.w, w.bias)
         assert torch.equal(moved.view(torch.int16), base[shift:].view(torch.int16)), shift
 
