@@ -1,19 +1,23 @@
 """Benchmark of the packed varlen attention hot path on GB300.
 
-One step = one pass of the whole path over one batch of the mixed-resolution
-joint text+image workload (4 requests: text U[16,256] + 2304/4096/6889/16384
-image tokens, H=24, D=128, bf16 N(0,1)):
+One step = one pass of the whole varlen path over one batch:
   cu_seqlens from lengths -> pack q, k, v (padded -> flat) -> varlen
   attention -> unpack the output (flat -> padded).
+The headline workload is the largest single-GPU config, the dynamic step
+batch with classifier-free guidance (8 requests with image tokens from
+{2304, 4096, 6889, 16384}, each doubled into a positive and a negative text
+span: 16 sequences, 129,490 tokens, H=24, D=128, bf16 N(0,1)).  The single
+edit request (256 + 32,768 tokens) and the mixed-resolution batch (4
+requests) are timed the same way and reported under "configs".
 The Token2Wav block-window variant (22 layers, n=2400, H=16, D=64, block 24)
 is timed in the same run and reported under "block_window", and its fp32
 form (the DiT's own dtype, classifier-free guidance as batch 2) under
 "block_window_f32".
 
 Rank 0 prints one JSON line.  Under torchrun each rank runs its own batch
-(seed + rank) on its own GPU; no data moves between ranks (weak scaling);
-the timed region is bracketed by a barrier and the slowest rank's time is
-reported.
+(its own value seed) on its own GPU; no data moves between ranks (weak
+scaling); the timed region is bracketed by a barrier and the slowest rank's
+time is reported.
 
 --impl reference times the CPU oracle (fp64 NumPy) on a bounded sample of the
 same workload on the host cores.
@@ -42,7 +46,11 @@ import workloads  # noqa: E402
 
 METRIC = "packed varlen attention useful TFLOP/s and % of GB300 bf16 tensor peak"
 UNIT = "TFLOP/s"
-WORKLOAD = "mixed_res_mmdit"
+WORKLOAD = "cfg_dynamic_batch"
+SUB_WORKLOADS = ("single_edit", "mixed_res_mmdit")
+# query rows per sequence of the CPU-oracle baseline sample, per workload
+# (about 5-15 s of fp64 work each on 16 host cores)
+CPU_ROWS = {"cfg_dynamic_batch": 512, "single_edit": 1024, "mixed_res_mmdit": 1024}
 # FP32 FMA rate of one GB300: 152 SMs x 128 lanes x 2 FLOP x 2.07 GHz
 FP32_PEAK_TFLOPS = 152 * 128 * 2 * 2.07e9 / 1e12
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
@@ -104,11 +112,11 @@ def _kernel_digest() -> str:
     return h.hexdigest()[:16]
 
 
-def _profiled(digest: str):
-    """Figures of the attention kernel from the committed ncu summary (DRAM
-    bytes per launch, tensor-pipe utilisation, DRAM GB/s), if it was taken on
-    the current kernel sources; else an empty dict."""
-    path = os.path.join(ROOT, "profiles", "varlen_attn_mixed_res_mmdit.md")
+def _profiled(digest: str, workload: str = WORKLOAD):
+    """Figures of the attention kernel on `workload` from its committed ncu
+    summary (DRAM bytes per launch, tensor-pipe utilisation, DRAM GB/s), if
+    it was taken on the current kernel sources; else an empty dict."""
+    path = os.path.join(ROOT, "profiles", f"varlen_attn_{workload}.md")
     try:
         text = open(path).read()
     except OSError:
@@ -122,10 +130,6 @@ def _profiled(digest: str):
         if m:
             out[key] = float(m.group(1))
     return out
-
-
-def _profiled_traffic(digest: str):
-    return _profiled(digest).get("dram_bytes_per_launch")
 
 
 def rank_seed(rank: int, base: int = 1002) -> int:
@@ -225,24 +229,26 @@ def block_window_flops(n, H, D, block, look_back, look_ahead):
     return 4 * H * D * pairs
 
 
-def oracle_sample(w, rows_per_seq: int, seed: int = 0):
-    """Bounded oracle sample: ``rows_per_seq`` query rows of every sequence,
-    all heads.  Returns (seconds, useful FLOPs of the sample, description)."""
+def oracle_sample(pw, rows_per_seq: int, seed: int = 0):
+    """Bounded oracle sample on a padded workload: ``rows_per_seq`` random
+    query rows of every sequence, all heads, against all of its keys; one
+    sequence at a time so only that sequence is held in fp64.  Returns
+    (seconds, useful FLOPs of the sample, description)."""
     import oracle
     rng = np.random.default_rng(seed)
-    cu = oracle.cu_seqlens_from_lengths(w.lengths_q)
-    rows, flops = [], 0
-    for b, L in enumerate(w.lengths_q):
-        r = np.sort(rng.choice(L, size=min(rows_per_seq, L), replace=False)) + cu[b]
-        rows.append(r)
-        flops += 4 * w.H * w.D * len(r) * w.lengths_k[b]
-    rows = np.concatenate(rows)
-    q, k, v = oracle.to_f64(w.q), oracle.to_f64(w.k), oracle.to_f64(w.v)
-    t0 = time.perf_counter()
-    oracle.varlen_attention(q, k, v, cu, cu, w.scale, rows=rows)
-    dt = time.perf_counter() - t0
-    desc = (f"{rows_per_seq} query rows per sequence x all {w.H} heads "
-            f"({len(rows)} rows) of the {w.name} batch, fp64 NumPy")
+    H, D = pw.H, pw.D
+    scale = 1.0 / math.sqrt(D)
+    flops, n_rows, dt = 0, 0, 0.0
+    for b, L in enumerate(pw.lengths):
+        r = np.sort(rng.choice(L, size=min(rows_per_seq, L), replace=False))
+        q, k, v = (oracle.to_f64(t[b, :L]) for t in (pw.q, pw.k, pw.v))
+        t0 = time.perf_counter()
+        oracle.varlen_attention(q, k, v, [0, L], [0, L], scale, rows=r)
+        dt += time.perf_counter() - t0
+        flops += 4 * H * D * len(r) * L
+        n_rows += len(r)
+    desc = (f"{rows_per_seq} query rows per sequence x all {H} heads ({n_rows} rows) of the "
+            f"{pw.name[:-len('_padded')]} batch against all keys, fp64 NumPy")
     return dt, flops, desc
 
 
@@ -250,13 +256,13 @@ def run_reference(args):
     ws, rank, _ = _dist_env()
     if rank != 0:
         return 0
-    w = workloads.mixed_res(seed=2)
+    pw = workloads.varlen_padded(WORKLOAD, rank_seed(0))
     rows = args.ref_rows
     for _ in range(args.warmup):
-        oracle_sample(w, rows)
+        oracle_sample(pw, rows)
     times, flops, desc = [], 0, ""
     for i in range(args.steps):
-        dt, flops, desc = oracle_sample(w, rows, seed=i)
+        dt, flops, desc = oracle_sample(pw, rows, seed=i)
         times.append(dt)
     total = sum(times)
     value = flops * args.steps / total / 1e12
@@ -266,8 +272,8 @@ def run_reference(args):
         "n_gpus": ws, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": 1e3 * total / args.steps, "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": WORKLOAD, "batch": len(w.lengths_q), "H": w.H, "D": w.D,
-                   "tokens": sum(w.lengths_q), "sample": desc},
+        "config": {"workload": WORKLOAD, "batch": len(pw.lengths), "H": pw.H, "D": pw.D,
+                   "tokens": sum(pw.lengths), "sample": desc},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": cores, "kind": "oracle",
                          "sample": desc},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -276,23 +282,12 @@ def run_reference(args):
     return 0
 
 
-def run_ours(args):
-    import packed_varlen_gb300 as pv
-
-    ws, rank, local = _dist_env()
-    if not torch.cuda.is_available():
-        raise RuntimeError("bench.py needs a CUDA GPU")
-    torch.cuda.set_device(local)
-    dev = torch.device("cuda", local)
-    dist = None
-    if ws > 1:
-        import torch.distributed as dist
-        dist.init_process_group("nccl", device_id=dev)
-    pv.load_library()
-    pv.get_device_status()
-
-    # ---- inputs: this rank's padded batch, resident in HBM -------------------
-    pw = workloads.mixed_res_padded(seed=2, value_seed=rank_seed(rank))
+def measure_varlen_config(pv, name, dev, args, flusher, rank, dist, ws, cpu_rows=None):
+    """Time K steps of the varlen path on one config, inputs resident in HBM
+    and L2 emptied between steps (outside the events); then the same K steps
+    end to end with host buffers; then, if asked, the CPU oracle on a bounded
+    sample.  Returns the fields of a bench line for this config."""
+    pw = workloads.varlen_padded(name, rank_seed(rank))
     L = pw.lengths
     T, H, D, B, S = sum(L), pw.H, pw.D, len(L), pw.s_max
     flops = 4 * H * D * sum(x * x for x in L)
@@ -303,9 +298,7 @@ def run_ours(args):
     qf = torch.empty(T, H, D, dtype=torch.bfloat16, device=dev)
     kf, vf, of = torch.empty_like(qf), torch.empty_like(qf), torch.empty_like(qf)
     out_pad = torch.zeros_like(q_pad)
-    flusher = L2Flusher(dev)
     scale = 1.0 / math.sqrt(D)
-
     attn_ev = []
 
     def step(record=False):
@@ -323,15 +316,15 @@ def run_ours(args):
         pv.unpack(of, cu, out_pad)
 
     launches_per_step = 6
-
-    for _ in range(max(3, args.warmup)):
+    warm = max(3, args.warmup)
+    for _ in range(warm):
         step()
     torch.cuda.synchronize()
     if pv.get_device_status() != 0:
-        raise RuntimeError("device status error during warm-up")
+        raise RuntimeError(f"device status error during the {name} warm-up")
 
     # ---- timed: K steps, L2 flushed between steps (outside the events) ------
-    sampler = ClockSampler(local)
+    sampler = ClockSampler(dev.index)
     sampler.start()
     time.sleep(0.3)
     if dist:
@@ -349,16 +342,94 @@ def run_ours(args):
     if dist:
         dist.barrier()
     clocks = sampler.stop()
+    if pv.get_device_status() != 0:
+        raise RuntimeError(f"device status error during the {name} timed steps")
     step_ms = [a.elapsed_time(b) for a, b in step_ev]
     attn_ms = [a.elapsed_time(b) for a, b in attn_ev]
     total_ms = max_over_ranks(sum(step_ms), dist, dev)
     value = flops * ws * args.steps / (total_ms * 1e-3) / 1e12
+    want_out = out_pad.cpu()
+    del q_pad, k_pad, v_pad, qf, kf, vf, of, out_pad
 
     # ---- end to end: host buffers in, host result out ----------------------
     # the same job size as the device-timed value: K steps, copies included
-    e2e_mean, h2d, d2h = run_e2e(pv, pw, L, dev, scale, max(3, args.steps), out_pad.cpu())
+    e2e_mean, h2d, d2h = run_e2e(pv, pw, dev, scale, max(3, args.steps), want_out)
     e2e_mean = max_over_ranks(e2e_mean, dist, dev)
     e2e_value = flops * ws / (e2e_mean * 1e-3) / 1e12
+    del want_out
+
+    peaks, peak_src = _peaks()
+    attn_mean_ms = statistics.mean(attn_ms)
+    achieved = flops / (attn_mean_ms * 1e-3) / 1e12
+    digest = _kernel_digest()
+    prof = _profiled(digest, name)
+    cpu = None
+    if cpu_rows and rank == 0 and ws == 1:
+        dt, sflops, desc = oracle_sample(pw, cpu_rows)
+        cpu = {"value": sflops / dt / 1e12, "unit": UNIT, "cores": _cpu_cores(),
+               "kind": "oracle", "sample": desc, "seconds": dt}
+    res = {
+        "value": value, "unit": UNIT, "ms_per_step": total_ms / args.steps,
+        "config": {"workload": name, "batch": B, "lengths": L, "tokens": T, "H": H, "D": D,
+                   "s_max": S, "useful_flops_per_step": flops,
+                   "step": "cu_seqlens + pack q,k,v + varlen attention + unpack",
+                   "l2": "flushed between timed steps outside the events (512 MB write, then "
+                         "512 MB read so L2 holds clean lines); padded inputs 3 x %.0f MB also "
+                         "exceed L2" % (pw.q.numel() * 2 / 2**20),
+                   "parallelism": f"{ws} independent batches (one per GPU)"},
+        "pct_of_peak": 100.0 * value / peaks["bf16_tflops"],
+        "roofline": {"kernel": "varlen_attn_fwd", "bound": "tensor",
+                     "achieved": achieved, "peak": peaks["bf16_tflops"],
+                     "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                     "peak_source": f"{peak_src} bf16 dense (burst)",
+                     "launch_ms": attn_mean_ms, "traffic": prof.get("dram_bytes_per_launch"),
+                     "ncu": {"tensor_pipe_active_pct": prof.get("tensor_pipe_active_pct"),
+                             "dram_gbs": prof.get("dram_gbs"),
+                             "source": f"profiles/varlen_attn_{name}.md"} if prof else None,
+                     "kernel_digest": digest},
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_mean,
+                "how": "each sequence's real q/k/v rows from pinned host memory into the padded "
+                       "device layout, step, real output rows back to pinned host memory; "
+                       "copy-in/compute/copy-out on three streams, double-buffered, all K "
+                       "steps inside the timed region (the first copy-in and the last "
+                       "copy-out included)"},
+        "gpu_launches": launches_per_step * args.steps,
+        "clocks": clocks,
+    }
+    return res, pw
+
+
+def run_ours(args):
+    import packed_varlen_gb300 as pv
+
+    ws, rank, local = _dist_env()
+    if not torch.cuda.is_available():
+        raise RuntimeError("bench.py needs a CUDA GPU")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dist = None
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    pv.load_library()
+    pv.get_device_status()
+    flusher = L2Flusher(dev)
+    stream = torch.cuda.current_stream()
+    no_cpu = args.no_cpu_baseline
+
+    head, _ = measure_varlen_config(pv, WORKLOAD, dev, args, flusher, rank, dist, ws,
+                                    None if no_cpu else CPU_ROWS[WORKLOAD])
+    torch.cuda.empty_cache()
+    # the other two large varlen configs, one GPU only (each a bench-line
+    # object of its own; the scaling runs time the headline alone)
+    subs = {}
+    if ws == 1:
+        for name in SUB_WORKLOADS:
+            subs[name], _ = measure_varlen_config(pv, name, dev, args, flusher, rank, None, 1,
+                                                  None if no_cpu else CPU_ROWS[name])
+            torch.cuda.empty_cache()
 
     # ---- block-window variants (Token2Wav), timed per layer ------------------
     bw_meas = measure_block_window(pv, workloads.token2wav(), False, dev, flusher, stream)
@@ -366,60 +437,27 @@ def run_ours(args):
     bw_meas["graph"] = measure_block_window_graph(pv, workloads.token2wav(), False, dev, flusher)
     bw32_meas["graph"] = measure_block_window_graph(pv, workloads.token2wav_f32(), True, dev,
                                                     flusher)
-
     if pv.get_device_status() != 0:
-        raise RuntimeError("device status error during the timed run")
+        raise RuntimeError("device status error during the block-window runs")
     cfg_meas = measure_cfg_combine(dev, 3072, 10, 3)
     rope_meas = measure_rope(dev, 10, 3)
     linear_meas = measure_linear(dev, 10, 3)
 
-    peaks, peak_src = _peaks()
-    attn_mean_ms = statistics.mean(attn_ms)
-    achieved = flops / (attn_mean_ms * 1e-3) / 1e12
-    digest = _kernel_digest()
-    prof = _profiled(digest)
-    traffic = prof.get("dram_bytes_per_launch")
-    result = None
+    peaks, _ = _peaks()
     if rank == 0:
-        cpu = None
-        if ws == 1 and not args.no_cpu_baseline:
-            w = workloads.mixed_res(seed=2)
-            dt, sflops, desc = oracle_sample(w, args.cpu_rows)
-            cpu = {"value": sflops / dt / 1e12, "unit": UNIT, "cores": _cpu_cores(),
-                   "kind": "oracle", "sample": desc, "seconds": dt}
         result = {
-            "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+            "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": ws,
             "steps": args.steps, "warmup": max(3, args.warmup),
-            "ms_per_step": total_ms / args.steps, "higher_is_better": True,
+            "ms_per_step": head["ms_per_step"], "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "batch": B, "lengths": L, "tokens": T, "H": H,
-                       "D": D, "s_max": S, "useful_flops_per_step": flops,
-                       "step": "cu_seqlens + pack q,k,v + varlen attention + unpack",
-                       "l2": "flushed between timed steps outside the events (512 MB write, then "
-                             "512 MB read so L2 holds clean lines); "
-                             "padded inputs 3 x %.0f MB also exceed L2"
-                             % (q_pad.numel() * 2 / 2**20),
-                       "parallelism": f"{ws} independent batches (one per GPU)"},
-            "pct_of_peak": 100.0 * value / peaks["bf16_tflops"],
-            "roofline": {"kernel": "varlen_attn_fwd", "bound": "tensor",
-                         "achieved": achieved, "peak": peaks["bf16_tflops"],
-                         "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
-                         "peak_source": f"{peak_src} bf16 dense (burst)",
-                         "launch_ms": attn_mean_ms, "traffic": traffic,
-                         "ncu": {"tensor_pipe_active_pct": prof.get("tensor_pipe_active_pct"),
-                                 "dram_gbs": prof.get("dram_gbs"),
-                                 "source": "profiles/varlen_attn_mixed_res_mmdit.md"}
-                         if prof else None,
-                         "kernel_digest": digest},
-            "cpu_baseline": cpu,
-            "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": e2e_mean,
-                    "how": "real rows of padded q/k/v from pinned host memory, step, real "
-                           "output rows back; copy-in/compute/copy-out on three streams, "
-                           "double-buffered, all K steps inside the timed region (the first "
-                           "copy-in and the last copy-out included)"},
-            "gpu_launches": launches_per_step * args.steps,
-            "clocks": clocks,
+            "config": head["config"],
+            "pct_of_peak": head["pct_of_peak"],
+            "roofline": head["roofline"],
+            "cpu_baseline": head["cpu_baseline"],
+            "e2e": head["e2e"],
+            "gpu_launches": head["gpu_launches"],
+            "clocks": head["clocks"],
+            "configs": subs,
             "block_window": dict(bw_meas, hbm_frac_own_block_layer=bw_meas["gbs_own_block_layer"]
                                  / peaks["hbm_gbs"],
                                  hbm_frac_graph=bw_meas["graph"]["gbs"] / peaks["hbm_gbs"]),
@@ -491,22 +529,27 @@ def run_attn_only(args):
     return 0
 
 
-def run_e2e(pv, pw, L, dev, scale, steps, want_out):
+def run_e2e(pv, pw, dev, scale, steps, want_out):
     """The same step through the public API with host buffers, pipelined the
-    way a serving loop would run it: each step copies its sequences' real
-    rows (padding rows are never read by the pack step, so they are not
-    sent) from pinned host memory, computes, and copies the real output rows
-    back to pinned host memory.  Copy-in, compute and copy-out run on three
-    streams with double-buffered device and host buffers, so step i+1's
-    copy-in overlaps step i's compute.  Returns (ms per step, H2D bytes per
-    step, D2H bytes per step); the timed region spans all steps' copies."""
+    way a serving loop would run it: each step copies every sequence's real
+    q/k/v rows (what a request holds; the pack step never reads padding rows)
+    from pinned host memory into the padded device layout, computes, and
+    copies the real output rows back to pinned host memory.  Copy-in,
+    compute and copy-out run on three streams with double-buffered device
+    and output buffers, so step i+1's copy-in overlaps step i's compute.
+    Returns (ms per step, H2D bytes per step, D2H bytes per step); the timed
+    region spans all steps' copies."""
+    L = pw.lengths
     B, S, H, D = len(L), pw.s_max, pw.H, pw.D
     row = H * D * 2
     T = sum(L)
-    host_in = [[t.pin_memory() for t in (pw.q, pw.k, pw.v)] for _ in range(2)]
+    # per request: its own pinned [L_b, H, D] q, k, v (read-only, shared by
+    # both pipeline buffers) and two pinned output buffers
+    host_in = [[t[j, :L[j]].pin_memory() for j in range(B)] for t in (pw.q, pw.k, pw.v)]
     host_len = torch.tensor(L, dtype=torch.int32).pin_memory()
-    host_out = [torch.empty((B, S, H, D), dtype=torch.bfloat16).pin_memory() for _ in range(2)]
-    dev_in = [[torch.empty((B, S, H, D), dtype=torch.bfloat16, device=dev) for _ in range(3)]
+    host_out = [[torch.empty((L[j], H, D), dtype=torch.bfloat16).pin_memory() for j in range(B)]
+                for _ in range(2)]
+    dev_in = [[torch.zeros((B, S, H, D), dtype=torch.bfloat16, device=dev) for _ in range(3)]
               for _ in range(2)]
     dev_len = [torch.empty(B, dtype=torch.int32, device=dev) for _ in range(2)]
     dev_out = [torch.zeros((B, S, H, D), dtype=torch.bfloat16, device=dev) for _ in range(2)]
@@ -528,7 +571,7 @@ def run_e2e(pv, pw, L, dev, scale, steps, want_out):
             dev_len[b].copy_(host_len, non_blocking=True)
             for t in range(3):
                 for j in range(B):
-                    dev_in[b][t][j, :L[j]].copy_(host_in[b][t][j, :L[j]], non_blocking=True)
+                    dev_in[b][t][j, :L[j]].copy_(host_in[t][j], non_blocking=True)
             ev_in[b].record(s_in)
         with torch.cuda.stream(s_cmp):
             s_cmp.wait_event(ev_in[b])
@@ -544,7 +587,7 @@ def run_e2e(pv, pw, L, dev, scale, steps, want_out):
         with torch.cuda.stream(s_out):
             s_out.wait_event(ev_cmp[b])
             for j in range(B):
-                host_out[b][j, :L[j]].copy_(dev_out[b][j, :L[j]], non_blocking=True)
+                host_out[b][j].copy_(dev_out[b][j, :L[j]], non_blocking=True)
             ev_out[b].record(s_out)
         first[b] = False
 
@@ -562,7 +605,7 @@ def run_e2e(pv, pw, L, dev, scale, steps, want_out):
     # the pipelined path must reproduce the plain step's output bit for bit
     got = host_out[(steps - 1) % 2]
     for j in range(B):
-        if not torch.equal(got[j, :L[j]].view(torch.int16), want_out[j, :L[j]].view(torch.int16)):
+        if not torch.equal(got[j].view(torch.int16), want_out[j, :L[j]].view(torch.int16)):
             raise RuntimeError("pipelined end-to-end output differs from the device step")
     return e0.elapsed_time(e1) / steps, h2d, d2h
 
@@ -817,9 +860,7 @@ def main():
     ap.add_argument("--steps", type=int, default=20)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--cpu-rows", type=int, default=2048,
-                    help="query rows per sequence in the CPU-oracle baseline sample")
-    ap.add_argument("--ref-rows", type=int, default=128,
+    ap.add_argument("--ref-rows", type=int, default=64,
                     help="query rows per sequence per step of --impl reference")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--attn-only", action="store_true",

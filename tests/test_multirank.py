@@ -21,8 +21,7 @@ def _worker(rank, world, port, out):
     import bench
     import workloads
     seed = bench.rank_seed(rank)
-    g = torch.Generator().manual_seed(2)
-    lengths = workloads.lengths_mixed_res(g)
+    lengths = workloads.config_lengths(bench.WORKLOAD)
     # same lengths on every rank, different values
     pw = workloads.padded(lengths, 1, 8, seed)   # small H/D: shape logic only
     first = float(pw.q[0, 0, 0, 0])

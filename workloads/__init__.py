@@ -247,6 +247,39 @@ def mixed_res_padded(seed: int = 2, value_seed: Optional[int] = None) -> PaddedW
     return padded(L, 24, 128, vs, name="mixed_res_mmdit_padded")
 
 
+def config_lengths(name: str) -> List[int]:
+    """Sequence lengths of a named varlen config, drawn exactly as the flat
+    workload of that name draws them."""
+    if name == "tiny":
+        return lengths_tiny()
+    if name == "mixed_res_mmdit":
+        return lengths_mixed_res(torch.Generator().manual_seed(2))
+    if name == "single_edit":
+        return lengths_single_edit()
+    if name == "cfg_dynamic_batch":
+        return lengths_cfg_batch(torch.Generator().manual_seed(5))[0]
+    raise KeyError(name)
+
+
+def varlen_padded(name: str, value_seed: int) -> PaddedWorkload:
+    """A named varlen config in the padded [B, S_max, H, D] layout the pack
+    step reads, with S_max the longest sequence.  Only real rows are drawn:
+    from ``value_seed``, sequence by sequence, the q rows of every sequence,
+    then k, then v; padding rows are zero.  (Drawing only the real rows keeps
+    the host cost of the 121k-token CFG batch to its 121k rows.)"""
+    L = config_lengths(name)
+    H, D = (2, 64) if name == "tiny" else (24, 128)
+    g = torch.Generator().manual_seed(value_seed)
+    s = max(L)
+    out = []
+    for _ in range(3):
+        t = torch.zeros((len(L), s, H, D), dtype=torch.bfloat16)
+        for b, n in enumerate(L):
+            t[b, :n] = _randn_bf16(g, (n, H, D))
+        out.append(t)
+    return PaddedWorkload(name + "_padded", list(L), s, H, D, out[0], out[1], out[2], value_seed)
+
+
 def random_varlen(lengths_q: List[int], lengths_k: Optional[List[int]], H: int, D: int,
                   seed: int, name: str = "random") -> VarlenWorkload:
     """Arbitrary lengths (tests): flat q [sum Lq, H, D], k/v [sum Lk, H, D]."""
