@@ -92,3 +92,38 @@ def test_graph_replay_matches_eager(pv):
     torch.cuda.synchronize()
     for a, b in zip(eager, outs):
         assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("D", [64, 128])
+@pytest.mark.parametrize("n,look", [(2390, (1, 1)), (101, (0, 0)), (333, (1, 2))])
+def test_batch_entries_do_not_leak(pv, D, n, look):
+    # entry 1 is all NaN / +-Inf: entry 0 (whose last blocks end where entry
+    # 1 begins in memory) must equal its run alone bit for bit and the oracle
+    w = workloads.random_block_window(2, n, 2, D, 24, seed=n + D)
+    bad = [t.clone() for t in (w.q, w.k, w.v)]
+    vals = torch.tensor([float("nan"), float("inf"), float("-inf")], dtype=torch.bfloat16)
+    for t in bad:
+        t[1] = vals.repeat(t[1].numel() // 3 + 1)[:t[1].numel()].view(t[1].shape)
+    w2 = workloads.BlockWindowWorkload("poisoned", 2, n, 2, D, 24, [look], *bad, w.seed)
+    got = _run(pv, w2, *look)
+    one = workloads.BlockWindowWorkload("alone", 1, n, 2, D, 24, [look], w.q[:1].contiguous(),
+                                        w.k[:1].contiguous(), w.v[:1].contiguous(), w.seed)
+    alone = _run(pv, one, *look)
+    assert torch.equal(got[0].view(torch.int16), alone[0].view(torch.int16))
+    want = oracle.block_window_attention(w.q[:1], w.k[:1], w.v[:1], 24, look[0], look[1],
+                                         w.scale)
+    assert_close_to_oracle(oracle.to_f64(got[:1]), want, f"entry 0 n={n} look={look} D={D}")
+    assert pv.get_device_status() == 0
+
+
+@pytest.mark.parametrize("block,n,look", [(24, 2400, (0, 0)), (24, 2400, (1, 1)),
+                                          (128, 1000, (1, 1)), (300, 1200, (0, 1)),
+                                          (5, 700, (9, 0))])
+def test_window_shapes_against_oracle(pv, block, n, look):
+    # single-chunk and multi-chunk windows (a window above 256 keys is taken
+    # in 256-key chunks with an online softmax), H = 16 like the DiT
+    w = workloads.random_block_window(1, n, 16, 64, block, seed=block * 7 + n)
+    got = oracle.to_f64(_run(pv, w, *look))
+    want = oracle.block_window_attention(w.q, w.k, w.v, block, look[0], look[1], w.scale)
+    assert_close_to_oracle(got, want, f"block={block} n={n} look={look}")
+    assert pv.get_device_status() == 0
