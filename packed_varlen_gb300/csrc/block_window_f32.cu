@@ -11,17 +11,17 @@
 // already a power of two and the exponentials are the hardware ex2.
 //
 // Work split.  Rows of one block share one key window, so a warp task is a
-// run of at most kRows rows inside one block.  kSplit = 2 lanes share a
-// group of kRL rows and each owns D / 2 of their dimensions (float4 slots i
-// with i % 2 == its part): D = 64 takes two rows per lane pair (kRL = 2,
-// 32 rows a task), D = 128 one (kRL = 1, 16 rows a task).  A lane keeps
-// its q slices and output accumulators in registers.  The window's keys are
-// the same for the whole warp, so every K or V load is a broadcast of two
-// adjacent 16-byte words; such a 128-bit load costs two shared-memory
-// wavefronts (512 bytes reach the warp's registers), and with kRL = 2 each
-// loaded float feeds two FMAs, which keeps shared memory at the FP32 pipes'
-// rate.  The online softmax runs per lane and row; one shuffle finishes a
-// score.
+// run of at most kRows rows inside one block.  kSplit lanes share a group of
+// kRL rows and each owns D / kSplit of their dimensions (float4 slots i with
+// i % kSplit == its part).  D = 64: kSplit = 4, kRL = 3, so a task is 24
+// rows, one 24-frame block on all 32 lanes (a two-lane split left 8 of 32
+// lanes idle on such blocks), and each float loaded from K or V feeds three
+// FMAs.  D = 128: kSplit = 2, kRL = 1, 16 rows a task.  A lane keeps its q
+// slices and output accumulators in registers.  The window's keys are the
+// same for the whole warp, so every K or V load is a broadcast of kSplit
+// adjacent 16-byte words.  The online softmax runs per lane and row;
+// log2(kSplit) shuffles finish a score.  K/V stages hold 12 keys for D = 64
+// (24- and 72-key windows fill them exactly) and 16 for D = 128.
 //
 // Pipeline.  Every warp is its own pipeline: it owns a run of consecutive
 // tasks and streams, for each, the task's q rows and then its window in
@@ -40,7 +40,6 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kStage = 16;    // keys per K/V stage (a multiple of kGroup)
 constexpr int kBuf = 3;       // ring slots per warp
 
 struct BwF32Params {
@@ -61,6 +60,9 @@ struct Task {
   int64_t off;
   int row_lo, row_hi, lo, hi;
 };
+
+template <int D>
+struct F32Shape;
 
 template <int kRows, int D>
 __device__ __forceinline__ Task task_of(const BwF32Params &p, int64_t T) {
@@ -84,6 +86,7 @@ __device__ __forceinline__ Task task_of(const BwF32Params &p, int64_t T) {
   return k;
 }
 
+template <int kStage>
 __device__ __forceinline__ int kv_stages(const Task &k) {
   return (k.hi - k.lo + kStage - 1) / kStage;
 }
@@ -107,18 +110,23 @@ __device__ __forceinline__ float exp2_hw(float x) {
   return y;
 }
 
+// D = 64: four lanes share a group of three rows, 16 dimensions each, so a
+// warp task is 24 rows: one 24-frame block on all 32 lanes, and every float
+// loaded from K or V feeds three FMAs.  D = 128: two lanes share one row.
 template <int D>
 struct F32Shape {
-  static constexpr int kSplit = 2;                  // lanes per row group
-  static constexpr int kRL = D == 64 ? 2 : 1;       // rows per lane
+  static constexpr int kSplit = D == 64 ? 4 : 2;    // lanes per row group
+  static constexpr int kRL = D == 64 ? 3 : 1;       // rows per lane
   static constexpr int kRows = 32 / kSplit * kRL;   // rows per warp task
-  static constexpr int kGroup = 8 / kRL;            // keys per online-softmax update
+  static constexpr int kGroup = D == 64 ? 4 : 8;    // keys per online-softmax update
+  static constexpr int kStage = D == 64 ? 12 : 16;  // keys per K/V stage (whole groups)
 };
 
 template <int D>
 __global__ void __launch_bounds__(kThreads) block_window_f32_kernel(const BwF32Params p) {
   using S = F32Shape<D>;
   constexpr int kSplit = S::kSplit, kRL = S::kRL, kRows = S::kRows, kGroup = S::kGroup;
+  constexpr int kStage = S::kStage;
   constexpr int kD4 = D / 4;                  // float4 per row
   constexpr int kF4 = kD4 / kSplit;           // float4 slots per lane and row
   constexpr int kSlot = 2 * kStage * D;       // floats per ring slot: K and V of a stage
@@ -164,7 +172,7 @@ __global__ void __launch_bounds__(kThreads) block_window_f32_kernel(const BwF32P
           cp_async16(dst + kStage * D + j * D + 4 * c, p.v + src, ok);
         }
       }
-      if (++is > kv_stages(ti)) {
+      if (++is > kv_stages<kStage>(ti)) {
         is = 0;
         if (++it < t_end) ti = task_of<kRows, D>(p, it);
       }
@@ -189,7 +197,7 @@ __global__ void __launch_bounds__(kThreads) block_window_f32_kernel(const BwF32P
     const float *cur = ring + slot * kSlot;
     if (cs == 0) {
       tc = task_of<kRows, D>(p, ct);
-      n_kv = kv_stages(tc);
+      n_kv = kv_stages<kStage>(tc);
       const float2 s2 = make_float2(p.q_scale, p.q_scale);
 #pragma unroll
       for (int rr = 0; rr < kRL; ++rr) {
@@ -237,7 +245,8 @@ __global__ void __launch_bounds__(kThreads) block_window_f32_kernel(const BwF32P
 #pragma unroll
           for (int kk = 0; kk < kGroup; ++kk) {
             float x = sc2[rr][kk].x + sc2[rr][kk].y;
-            x += __shfl_xor_sync(0xffffffffu, x, 1);
+#pragma unroll
+            for (int sh = 1; sh < kSplit; sh <<= 1) x += __shfl_xor_sync(0xffffffffu, x, sh);
             pr[rr][kk] = g + kk < e ? x : -INFINITY;   // keys past e: zero-filled rows
           }
           float mx = pr[rr][0];
@@ -312,7 +321,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 template <int D>
 cudaError_t launch_f32(BwF32Params p, int batch, int H, cudaStream_t st) {
   constexpr int kRows = F32Shape<D>::kRows;
-  constexpr int kSmem = kWarps * kBuf * 2 * kStage * D * 4;
+  constexpr int kSmem = kWarps * kBuf * 2 * F32Shape<D>::kStage * D * 4;
   static unsigned long long done = 0;
   cudaError_t e = set_smem_once(reinterpret_cast<const void *>(&block_window_f32_kernel<D>),
                                 kSmem, done);
