@@ -382,6 +382,11 @@ def measure_varlen_config(pv, name, dev, args, flusher, rank, dist, ws, cpu_rows
                      "achieved": achieved, "peak": peaks["bf16_tflops"],
                      "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
                      "peak_source": f"{peak_src} bf16 dense (burst)",
+                     # context: the same launch against the power-capped
+                     # sustained GEMM rate (back-to-back steps run the GPU
+                     # at its power limit; the headline fraction is the
+                     # burst one above)
+                     "frac_of_sustained": achieved / peaks["bf16_tflops_sustained"],
                      "launch_ms": attn_mean_ms, "traffic": prof.get("dram_bytes_per_launch"),
                      "ncu": {"tensor_pipe_active_pct": prof.get("tensor_pipe_active_pct"),
                              "dram_gbs": prof.get("dram_gbs"),
