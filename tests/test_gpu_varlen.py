@@ -234,3 +234,17 @@ def test_nonfinite_neighbour_rows_do_not_leak(pv, D, lengths):
                                         rows=np.arange(s2, s2 + lengths[2]))
         assert_close_to_oracle(oracle.to_f64(packed[s2:s2 + lengths[2]]), want2, "sequence 2")
     assert pv.get_device_status() == 0
+
+
+@pytest.mark.slow
+def test_mixed_batch_every_row_of_two_heads(pv):
+    # every query row of heads 0 and 23 of the full mixed-resolution batch
+    # against the oracle; heads are independent, so the oracle runs on those
+    # two heads' slices of q, k and v
+    w = workloads.mixed_res()
+    out, cu_q, _ = gpu_varlen(pv, w)
+    cu = oracle.cu_seqlens_from_lengths(w.lengths_q)
+    heads = [0, w.H - 1]
+    want = oracle.varlen_attention(w.q[:, heads], w.k[:, heads], w.v[:, heads], cu, cu, w.scale)
+    assert_close_to_oracle(oracle.to_f64(out[:, heads]), want, "mixed batch, heads 0 and 23")
+    assert pv.get_device_status() == 0
