@@ -127,3 +127,39 @@ def test_window_shapes_against_oracle(pv, block, n, look):
     want = oracle.block_window_attention(w.q, w.k, w.v, block, look[0], look[1], w.scale)
     assert_close_to_oracle(got, want, f"block={block} n={n} look={look}")
     assert pv.get_device_status() == 0
+
+
+def test_chained_layers_respect_stream_order(pv):
+    # The kernel is launched so that it may start while the previous kernel
+    # on the stream drains; its copies and stores must still wait for that
+    # kernel.  Layer i reads layer i-1's output (read after write), and in
+    # the second chain each layer writes over the buffer the previous layer
+    # read (write after read).  No host sync between launches; the result
+    # must equal the same chain run with a sync after every launch.
+    w = workloads.token2wav(n=2400)
+    q, k, v = w.q.cuda(), w.k.cuda(), w.v.cuda()
+    looks = [(0, 0), (1, 1), (0, 0), (1, 1), (0, 0)]
+
+    def chain(sync):
+        x = q.clone()
+        for lb, la in looks:
+            x = pv.block_window_attn_fwd(x, k, v, w.block, lb, la)
+            if sync:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        return x
+
+    def chain_in_place(sync):
+        a, b = q.clone(), torch.empty_like(q)
+        for lb, la in looks:
+            pv.block_window_attn_fwd(a, k, v, w.block, lb, la, out=b)
+            a, b = b, a   # the next layer writes over the buffer just read
+            if sync:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        return a
+
+    assert torch.equal(chain(False).view(torch.int16), chain(True).view(torch.int16))
+    assert torch.equal(chain_in_place(False).view(torch.int16),
+                       chain_in_place(True).view(torch.int16))
+    assert pv.get_device_status() == 0
