@@ -6,6 +6,10 @@
 // varlen attention for mixfusion", Key changes; "feat: Support dynamic
 // batching for heterogeneous diffusion requests", AttentionMetadata).
 //
+// This kernel serves head dim 64; head dim 128 runs on the CTA-pair kernel
+// (attn_pair.cu), whose M = 256 MMAs leave TMEM room to compute scores
+// ahead of the softmax.
+//
 // Design: one persistent CTA per SM, 11 warps.  A work item is 256 query
 // rows of one (sequence, head), held as two 128-row tiles Q0 and Q1 that share
 // every K/V tile loaded, so each K/V byte brought into shared memory feeds
@@ -638,12 +642,11 @@ cudaError_t launch_tc(const VarlenArgs &a, cudaStream_t stream) {
 
 }  // namespace
 
-// Ring depth: with D = 128 a fifth 32 KB slot fits only beside a work list
-// of at most 256 sequences; larger batches use four slots.
+// Head dim 128 runs on the CTA-pair kernel; head dim 64 here, with a
+// ten-slot K/V ring beside a work list of up to PA_MAX_BATCH sequences.
 cudaError_t launch_varlen_attn(const VarlenArgs &a, cudaStream_t stream) {
-  if (a.D == 64) return launch_tc<64, 10, PA_MAX_BATCH>(a, stream);
-  if (a.batch <= 256) return launch_tc<128, 5, 256>(a, stream);
-  return launch_tc<128, 4, PA_MAX_BATCH>(a, stream);
+  if (a.D == 128) return launch_varlen_attn_pair(a, stream);
+  return launch_tc<64, 10, PA_MAX_BATCH>(a, stream);
 }
 
 }  // namespace pa

@@ -52,6 +52,7 @@ pa_status from_cuda(cudaError_t e);
 
 // Launchers: return cudaSuccess or the launch error.
 cudaError_t launch_varlen_attn(const VarlenArgs &a, cudaStream_t stream);
+cudaError_t launch_varlen_attn_pair(const VarlenArgs &a, cudaStream_t stream);   // D = 128
 cudaError_t launch_block_window_attn(const BlockWindowArgs &a, cudaStream_t stream);
 
 }  // namespace pa

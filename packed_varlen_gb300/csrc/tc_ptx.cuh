@@ -108,6 +108,16 @@ __device__ __forceinline__ void tma_load_2d_pair(uint32_t dst, const CUtensorMap
       : "memory");
 }
 
+// 3-D form of tma_load_2d_pair.
+__device__ __forceinline__ void tma_load_3d_pair(uint32_t dst, const CUtensorMap *map,
+                                                 uint32_t bar, int c0, int c1, int c2) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.cta_group::2.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%3, %4, %5}], [%2];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2)
+      : "memory");
+}
+
 // ---------------------------------------------------------------- clusters
 __device__ __forceinline__ uint32_t cluster_ctarank() {
   uint32_t r;
@@ -134,6 +144,24 @@ __device__ __forceinline__ void mbar_arrive_remote(uint32_t bar_cluster) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(bar_cluster)
                : "memory");
 }
+// The same arrival without release semantics (no memory barrier before it),
+// for signals that publish no generic-proxy memory: TMEM data written by
+// tcgen05.st and waited for with tcgen05.wait::st, or bytes that a copy
+// reports on the barrier itself.  A release at cluster scope would first
+// wait for every earlier store of the thread.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t bar_cluster) {
+  asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(bar_cluster)
+               : "memory");
+}
+// mbar_arrive_remote_relaxed that also adds `bytes` to the barrier's
+// expected transaction count (for copies that complete on it).
+__device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t bar_cluster,
+                                                             uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;\n" ::"r"(
+                   bar_cluster),
+               "r"(bytes)
+               : "memory");
+}
 // try_wait with cluster-scope acquire: for barriers that other CTAs arrive on.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
   uint32_t ok;
@@ -145,6 +173,33 @@ __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t par
       : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
+}
+
+// bounded_wait with cluster-scope acquire (mbar_try_wait_cluster).
+__device__ __forceinline__ bool bounded_wait_cluster(uint32_t bar, uint32_t parity,
+                                                     volatile int32_t *abort_flag,
+                                                     int32_t *status, long long limit) {
+  if (mbar_try_wait_cluster(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (true) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if (clock64() - t0 > limit) {
+      *abort_flag = 1;
+      record_error(status, PA_DEVICE_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+// Named CTA barrier `id` (1..15) over `count` threads (a multiple of 32):
+// wait for all of them, or (arrive) count this warp in and go on.  The
+// writes a thread made before either are visible to the threads that waited.
+__device__ __forceinline__ void named_bar_sync(uint32_t id, uint32_t count) {
+  asm volatile("bar.sync %0, %1;\n" ::"r"(id), "r"(count) : "memory");
+}
+__device__ __forceinline__ void named_bar_arrive(uint32_t id, uint32_t count) {
+  asm volatile("bar.arrive %0, %1;\n" ::"r"(id), "r"(count) : "memory");
 }
 
 // ---------------------------------------------------------------- tcgen05
@@ -222,6 +277,17 @@ __device__ __forceinline__ void mma_ss_pair(uint32_t d_tmem, uint64_t a_desc, ui
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::2.kind::f16 [%0], %1, %2, %3, p;\n\t}\n" ::"r"(d_tmem),
       "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate));
+}
+
+// TS form of mma_ss_pair: A (M = 256 rows) from TMEM, each CTA's 128 rows in
+// its own TMEM at the same address.
+__device__ __forceinline__ void mma_ts_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate));
 }
 
 // Instruction descriptor of kind::f16: bf16 A and B, fp32 D, dense.

@@ -55,7 +55,8 @@ def test_cross_lengths_and_empty_keys(pv, lq, lk):
 
 @pytest.mark.parametrize("D", [64, 128])
 def test_many_sequences(pv, D):
-    # D = 128 with more than 256 sequences runs the 4-slot, 1024-sequence variant
+    # a long work list of short and empty sequences: many items per CTA (pair),
+    # single-tile items, items without keys between items with keys
     rng = np.random.default_rng(7)
     L = rng.integers(0, 200, size=300).tolist()
     w = workloads.random_varlen(L, None, 2, D, seed=8)
@@ -63,16 +64,41 @@ def test_many_sequences(pv, D):
 
 
 def test_every_item_single_tile(pv):
-    # no sequence reaches a second 128-row tile: the second MMA issuer only
-    # releases slots and never issues
+    # no sequence reaches a second 128-row tile: the odd CTA of each pair
+    # computes only rows past its item and stores none, and every item has a
+    # single key tile
     w = workloads.random_varlen([100, 50, 128, 7, 64, 128, 1], None, 3, 128, seed=12)
     _check_full(pv, w, "single-tile items")
 
 
-def test_max_batch(pv):
+@pytest.mark.parametrize("D", [64, 128])
+def test_max_batch(pv, D):
     L = ([1, 2, 0, 130] * 256)[:1024]
-    w = workloads.random_varlen(L, None, 1, 64, seed=9)
-    _check_full(pv, w, "1024 sequences")
+    w = workloads.random_varlen(L, None, 1, D, seed=9)
+    _check_full(pv, w, f"1024 sequences D={D}")
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_rescale_on_growing_scores(pv, D):
+    # Key rows grow with their key tile, so the row maximum jumps by far more
+    # than 2^8 between tiles and O is rescaled on most tiles (including a
+    # sequence's last tile and the last tiles of a CTA's stream); the tile
+    # order starts at a rotated tile, so maxima also stay flat for a while.
+    L = [700, 1300, 260]
+    w = workloads.random_varlen(L, None, 2, D, seed=21)
+    k = w.k.float()
+    start = 0
+    for n in L:
+        grow = 1.0 + 1.5 * (torch.arange(n, dtype=torch.float32) // 128)
+        k[start:start + n] *= grow[:, None, None]
+        start += n
+    w.k = k.to(torch.bfloat16)
+    for scale in (0.3, None):
+        out, _, _ = gpu_varlen(pv, w, scale=scale)
+        cu = oracle.cu_seqlens_from_lengths(w.lengths_q)
+        sc = w.scale if scale is None else scale
+        want = oracle.varlen_attention(w.q, w.k, w.v, cu, cu, sc)
+        assert_close_to_oracle(oracle.to_f64(out), want, f"growing scores D={D} scale={sc}")
 
 
 def test_scale_argument(pv):
