@@ -58,6 +58,7 @@ constexpr int kItemRows = 256;      // query rows per work item (one pair)
 constexpr int kCluster = 2;
 constexpr int kSBufs = 3;           // S/P buffers in TMEM
 constexpr int kThreads = 320;       // producer, MMA issuer, 8 softmax warps
+constexpr int kQBufs = 2;           // Q tile buffers
 constexpr int kSlots = 9;           // K/V ring slots
 constexpr long long kWaitLimit = 4000000000LL;  // clock cycles (~2 s)
 constexpr long long kDrainLimit = 400000000LL;  // teardown after an abort (~0.2 s)
@@ -68,17 +69,17 @@ struct PairCfg {
   static constexpr int kQBytes = 2 * kHalfBytes;    // one 128 x 128 Q tile
   static constexpr int kKHalfBytes = 64 * 128;      // 64 keys x 128 B
   static constexpr int kSlotBytes = 16384;          // a K half-tile or a V half-tile
-  static constexpr int kQOff = 0;                   // two Q buffers
-  static constexpr int kRingOff = 2 * kQBytes;
+  static constexpr int kQOff = 0;                   // kQBufs Q buffers
+  static constexpr int kRingOff = kQBufs * kQBytes;
   static constexpr int kBarOff = kRingOff + kSlots * kSlotBytes;
-  static constexpr int kQFull = 0,      // [2] even CTA: Q bytes of both CTAs
-      kQEmpty = 2,                      // [2] both: the item's last S is done
+  static constexpr int kQFull = 0,      // [kQBufs] even CTA: Q bytes of both CTAs
+      kQEmpty = 2,                      // [kQBufs] both: the item's last S is done
       kSFull = 4,                       // [3] both: S of a key tile is done
       kPReady = 7,                      // [3] even CTA: the pair's 8 warps of the tile wrote P
       kOFull = 10,                      // both: the item's last PV is done
       kFinal = 11,                      // even CTA: every MMA done (teardown)
       kTail = 12,                       // own: a V half-tile whose tail rows are cleared
-      kSlotFull = 13,                   // [kSlots] even CTA: both CTAs' bytes (2 arrivals)
+      kSlotFull = 13,                   // [kSlots] even CTA: both CTAs' bytes
       kSlotEmpty = 13 + kSlots;         // [kSlots] both
   static constexpr int kNumBars = 13 + 2 * kSlots;
   static constexpr int kMiscOff = kBarOff + kNumBars * 8;   // tmem base, abort flag
@@ -255,8 +256,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
 
   // ---- set-up: barriers, TMEM, work list --------------------------------
   if (tid == 0) {
-    for (int b = 0; b < 2; ++b) {
-      mbar_init(bar(C::kQFull + b), 2);    // each CTA's producer arrives with its bytes
+    for (int b = 0; b < kQBufs; ++b) {
+      mbar_init(bar(C::kQFull + b), 1);    // the even CTA's expect_tx; bytes of both CTAs
       mbar_init(bar(C::kQEmpty + b), 1);
     }
     for (int b = 0; b < kSBufs; ++b) {
@@ -267,7 +268,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     mbar_init(bar(C::kFinal), 1);
     mbar_init(bar(C::kTail), 1);
     for (int s = 0; s < kSlots; ++s) {
-      mbar_init(bar(C::kSlotFull + s), 2);
+      mbar_init(bar(C::kSlotFull + s), 1);   // as kQFull
       mbar_init(bar(C::kSlotEmpty + s), 1);
     }
     *abort_flag = 0;
@@ -306,11 +307,11 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
       return wait_all(bar(C::kSlotEmpty + s), ((loads / kSlots) & 1u) ^ 1u);
     };
     auto load_q = [&](const ItemInfo &it) -> bool {
-      const uint32_t qb = q_loads & 1u;
-      if (!wait_all(bar(C::kQEmpty + qb), ((q_loads >> 1) & 1u) ^ 1u)) return false;
+      const uint32_t qb = q_loads % kQBufs;
+      if (!wait_all(bar(C::kQEmpty + qb), ((q_loads / kQBufs) & 1u) ^ 1u)) return false;
       if (lead) {
         const uint32_t full = mapa_shared(bar(C::kQFull + qb), 0);
-        mbar_arrive_expect_tx_remote(full, C::kQBytes);
+        if (leader) mbar_arrive_expect_tx(bar(C::kQFull + qb), kCluster * C::kQBytes);
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf)
           tma_load_3d_pair(sQ + qb * C::kQBytes + hf * C::kHalfBytes, &tm_q, full, hf * 64,
@@ -326,7 +327,7 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
       const int row = w.it.k0 + key_tile(w.it, w.j) * kTile + static_cast<int>(rank) * 64;
       if (lead) {
         const uint32_t full = mapa_shared(bar(C::kSlotFull + s), 0);
-        mbar_arrive_expect_tx_remote(full, C::kSlotBytes);
+        if (leader) mbar_arrive_expect_tx(bar(C::kSlotFull + s), kCluster * C::kSlotBytes);
 #pragma unroll
         for (int hf = 0; hf < 2; ++hf)
           tma_load_3d_pair(sRing + s * C::kSlotBytes + hf * C::kKHalfBytes, &tm_k, full,
@@ -344,17 +345,15 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
       const int valid = w.it.lk - kt * kTile;
       const uint32_t dst = sRing + s * C::kSlotBytes;
       const uint32_t full = mapa_shared(bar(C::kSlotFull + s), 0);
+      if (lead && leader) mbar_arrive_expect_tx(bar(C::kSlotFull + s), kCluster * C::kSlotBytes);
       if (valid >= kTile) {
-        if (lead) {
-          mbar_arrive_expect_tx_remote(full, C::kSlotBytes);
-          tma_load_3d_pair(dst, &tm_v, full, static_cast<int>(rank) * 64, w.it.head, row);
-        }
+        if (lead) tma_load_3d_pair(dst, &tm_v, full, static_cast<int>(rank) * 64, w.it.head, row);
       } else {
         // The tile holds rows past the sequence end (the next sequence's, or
         // the buffer's trailing rows).  P is 0 there, but 0 * Inf and
         // 0 * NaN are NaN, so those rows are zeroed before the MMAs may read
         // the slot: the copy completes on this CTA's own barrier, the rows
-        // are cleared, and only then is the slot reported full.
+        // are cleared, and only then are its bytes counted on the slot.
         if (lead) {
           mbar_arrive_expect_tx(bar(C::kTail), C::kSlotBytes);
           tma_load_3d(dst, &tm_v, bar(C::kTail), static_cast<int>(rank) * 64, w.it.head, row);
@@ -365,16 +364,18 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
         ++tails;
         // one 64-column half: 128 rows x 128 B; the 128-byte swizzle only
         // permutes 16-byte chunks inside a row, so whole rows are cleared
-        // without unswizzling.  The fences order the stores after the TMA
-        // bytes and before the tensor core's reads (both async-proxy).
+        // without unswizzling.  The proxy fences order the stores after the
+        // TMA bytes and before the tensor core's reads (both async-proxy);
+        // the release fence publishes them to the even CTA's MMA issuer.
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
         uint8_t *tile = gbase + C::kRingOff + s * C::kSlotBytes;
         for (int c = lane; c < (kTile - valid) * 8; c += 32)
           *reinterpret_cast<uint4 *>(tile + (valid + (c >> 3)) * 128 + (c & 7) * 16) =
               make_uint4(0u, 0u, 0u, 0u);
         asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        fence_acq_rel_cluster();
         __syncwarp();
-        if (lead) mbar_arrive_remote(full);
+        if (lead) mbar_complete_tx_remote(full, C::kSlotBytes);
       }
       ++loads;
       return true;
@@ -404,8 +405,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
           const uint32_t n = (loads - s + kSlots - 1) / kSlots;  // loads into slot s
           drain_wait(bar(C::kSlotFull + s), (n - 1) & 1u, kDrainLimit);
         }
-        for (uint32_t b = 0; b < 2 && b < q_loads; ++b) {
-          const uint32_t n = (q_loads - b + 1) / 2;
+        for (uint32_t b = 0; b < static_cast<uint32_t>(kQBufs) && b < q_loads; ++b) {
+          const uint32_t n = (q_loads - b + kQBufs - 1) / kQBufs;   // loads into buffer b
           drain_wait(bar(C::kQFull + b), (n - 1) & 1u, kDrainLimit);
         }
       }
@@ -460,8 +461,8 @@ __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
           ++gs;
           return true;
         }
-        const uint32_t qb = kq & 1u;
-        if (kw.j == 0 && !wait_all(bar(C::kQFull + qb), (kq >> 1) & 1u)) return false;
+        const uint32_t qb = kq % kQBufs;
+        if (kw.j == 0 && !wait_all(bar(C::kQFull + qb), (kq / kQBufs) & 1u)) return false;
         uint32_t s;
         if (!next_slot(s)) return false;
         const uint64_t a0 = qdesc0 + ((qb * C::kQBytes) >> 4);

@@ -153,14 +153,18 @@ __device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t bar_cluster)
   asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];\n" ::"r"(bar_cluster)
                : "memory");
 }
-// mbar_arrive_remote_relaxed that also adds `bytes` to the barrier's
-// expected transaction count (for copies that complete on it).
-__device__ __forceinline__ void mbar_arrive_expect_tx_remote(uint32_t bar_cluster,
-                                                             uint32_t bytes) {
-  asm volatile("mbarrier.arrive.expect_tx.relaxed.cluster.shared::cluster.b64 _, [%0], %1;\n" ::"r"(
+// Counts `bytes` as arrived on an mbarrier of any CTA of the cluster, as a
+// copy completing on it would (for bytes that were declared with expect_tx
+// but delivered another way).  Relaxed: a release fence must precede it
+// where it publishes memory.
+__device__ __forceinline__ void mbar_complete_tx_remote(uint32_t bar_cluster, uint32_t bytes) {
+  asm volatile("mbarrier.complete_tx.relaxed.cluster.shared::cluster.b64 [%0], %1;\n" ::"r"(
                    bar_cluster),
                "r"(bytes)
                : "memory");
+}
+__device__ __forceinline__ void fence_acq_rel_cluster() {
+  asm volatile("fence.acq_rel.cluster;\n" ::: "memory");
 }
 // try_wait with cluster-scope acquire: for barriers that other CTAs arrive on.
 __device__ __forceinline__ bool mbar_try_wait_cluster(uint32_t bar, uint32_t parity) {
