@@ -72,9 +72,9 @@ constexpr int kGroups = 3;                       // softmax warpgroups
 constexpr int kThreads = (3 + 4 * kGroups) * 32; // producer, S issuer, softmax groups, PV issuer
 constexpr int kPvWarp = 2 + 4 * kGroups;
 constexpr int kTmemCols = 512;
-constexpr int kBarsPerSlot = 8;
-constexpr int kQFull = 0, kQEmpty = 1, kKvFull = 2, kKvEmpty = 3, kSFull = 4, kPReady = 5,
-              kOFull = 6, kTFree = 7;
+constexpr int kBarsPerSlot = 9;
+constexpr int kQFull = 0, kQEmpty = 1, kKFull = 2, kKvEmpty = 3, kSFull = 4, kPReady = 5,
+              kOFull = 6, kTFree = 7, kVFull = 8;
 constexpr int kBarBytes = (kMaxSlots * kBarsPerSlot + 2) * 8;
 constexpr int kMiscBytes = 16;                   // TMEM base, abort flag
 constexpr int kMaxSmem = 232448;
@@ -149,6 +149,29 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
       "r"(r[15])
       : "memory");
 }
+// TMEM -> registers, 32 lanes x 8 columns; registers -> TMEM, 32 lanes x 8
+// or 4 columns.  Each is used at a column offset that is a multiple of its
+// width.
+__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t *r) {
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t *r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(
+                   taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t *r) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(taddr),
+               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
+               : "memory");
+}
+constexpr int kFastCols = 32;   // widest window of the one-window fast path
+
 // Bounded mbarrier wait: the first poll inline, the polling loop out of
 // line (it only runs while the warp has nothing else to do), which keeps the
 // many wait sites of this short kernel from inflating its code.
@@ -238,7 +261,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     for (int s = 0; s < ns; ++s) {
       mbar_init(bar(s, kQFull), 1);
       mbar_init(bar(s, kQEmpty), 1);
-      mbar_init(bar(s, kKvFull), 1);
+      mbar_init(bar(s, kKFull), 1);
+      mbar_init(bar(s, kVFull), 1);
       mbar_init(bar(s, kKvEmpty), 1);
       mbar_init(bar(s, kSFull), 1);
       mbar_init(bar(s, kPReady), 128);
@@ -274,19 +298,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (warp == 0) {
     // ================= TMA producer =================
     const bool lead = elect_one();
-    uint32_t kvc[kMaxSlots] = {0, 0, 0, 0};
+    uint32_t kvc[kMaxSlots] = {0, 0, 0, 0};   // K copies per slot
+    uint32_t vc[kMaxSlots] = {0, 0, 0, 0};    // V copies per slot
     int q_loads = 0;
     bool ok = true;
     const uint32_t q_bytes = (G == 32 ? kM : 4u * G) * D * 2u;
-    const uint32_t kv_bytes = 2u * static_cast<uint32_t>(N) * D * 2u;
-    for (int li = 0; li < n_local && ok; ++li) {
+    const uint32_t kv_bytes = static_cast<uint32_t>(N) * D * 2u;   // K or V of one chunk
+    // Q of local item li, after the slot's previous item has released it
+    auto load_q = [&](int li, const BwItem &it) -> bool {
       const int s = li % ns;
-      const BwItem it = bw_item(p, blockIdx.x + li * gridDim.x);
       const uint32_t slot = base + s * p.slot_bytes;
-      if (!wait_all(bar(s, kQEmpty), ((li / ns) & 1) ^ 1)) {
-        ok = false;
-        break;
-      }
+      if (!wait_all(bar(s, kQEmpty), ((li / ns) & 1) ^ 1)) return false;
       if (li == 0) griddep_wait();
       if (lead) {
         mbar_arrive_expect_tx(bar(s, kQFull), q_bytes);
@@ -304,31 +326,63 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
       }
       ++q_loads;
-      for (int c = 0; c < it.nc; ++c) {
-        const uint32_t u = cnt_get(kvc, s);
-        if (!wait_all(bar(s, kKvEmpty), (u & 1u) ^ 1u)) {
-          ok = false;
-          break;
-        }
-        if (lead) {
-          mbar_arrive_expect_tx(bar(s, kKvFull), kv_bytes);
-          const int row = it.kb + c * N;
+      return true;
+    };
+    // K of chunk c, after the slot's previous chunk has released its K/V
+    auto load_k = [&](int s, const BwItem &it, int c) -> bool {
+      if (!wait_all(bar(s, kKvEmpty), (cnt_get(kvc, s) & 1u) ^ 1u)) return false;
+      if (lead) {
+        mbar_arrive_expect_tx(bar(s, kKFull), kv_bytes);
 #pragma unroll
-          for (int hf = 0; hf < D / 64; ++hf) {
-            tma_load_4d(slot + p.k_off + hf * (N * 128), &tm_k, bar(s, kKvFull), hf * 64, it.h,
-                        row, it.bi);
-            tma_load_4d(slot + p.v_off + hf * (N * 128), &tm_v, bar(s, kKvFull), hf * 64, it.h,
-                        row, it.bi);
-          }
+        for (int hf = 0; hf < D / 64; ++hf)
+          tma_load_4d(base + s * p.slot_bytes + p.k_off + hf * (N * 128), &tm_k, bar(s, kKFull),
+                      hf * 64, it.h, it.kb + c * N, it.bi);
+      }
+      cnt_add(kvc, s, 1u);
+      return true;
+    };
+    // V of chunk c (its slot was waited for by load_k)
+    auto load_v = [&](int s, const BwItem &it, int c) {
+      if (lead) {
+        mbar_arrive_expect_tx(bar(s, kVFull), kv_bytes);
+#pragma unroll
+        for (int hf = 0; hf < D / 64; ++hf)
+          tma_load_4d(base + s * p.slot_bytes + p.v_off + hf * (N * 128), &tm_v, bar(s, kVFull),
+                      hf * 64, it.h, it.kb + c * N, it.bi);
+      }
+      cnt_add(vc, s, 1u);
+    };
+    if constexpr (!kMulti) {
+      // One chunk per item.  Items go in windows of ns (one per slot); a
+      // window's Q and K copies are issued before its V copies.  The loads
+      // are DRAM-bound and land roughly in issue order, so the scores and
+      // softmax of every item of the window run while the V rows stream in,
+      // and only the PV and the epilogue follow the last bytes.
+      for (int w0 = 0; w0 < n_local && ok; w0 += ns) {
+        const int w1 = min(n_local, w0 + ns);
+        for (int li = w0; li < w1 && ok; ++li) {
+          const BwItem it = bw_item(p, blockIdx.x + li * gridDim.x);
+          ok = load_q(li, it) && load_k(li % ns, it, 0);
         }
-        cnt_add(kvc, s, 1u);
+        for (int li = w0; li < w1 && ok; ++li)
+          load_v(li % ns, bw_item(p, blockIdx.x + li * gridDim.x), 0);
+      }
+    } else {
+      for (int li = 0; li < n_local && ok; ++li) {
+        const BwItem it = bw_item(p, blockIdx.x + li * gridDim.x);
+        ok = load_q(li, it);
+        for (int c = 0; c < it.nc && ok; ++c) {
+          ok = load_k(li % ns, it, c);
+          if (ok) load_v(li % ns, it, c);
+        }
       }
     }
     if (!ok) {
       // give the copies already issued a bounded chance to land
       for (int s = 0; s < ns; ++s) {
-        const uint32_t u = cnt_get(kvc, s);
-        if (u) drain_wait(bar(s, kKvFull), (u - 1) & 1u, kDrainLimit);
+        const uint32_t u = cnt_get(kvc, s), uv = cnt_get(vc, s);
+        if (u) drain_wait(bar(s, kKFull), (u - 1) & 1u, kDrainLimit);
+        if (uv) drain_wait(bar(s, kVFull), (uv - 1) & 1u, kDrainLimit);
         const int qn = (q_loads + ns - 1 - s) / ns;   // Q loads into slot s
         if (qn) drain_wait(bar(s, kQFull), (qn - 1) & 1u, kDrainLimit);
       }
@@ -364,7 +418,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           const int s = li % ns;
           const uint32_t ph = (li / ns) & 1;
           if (!wait_all(bar(s, kQFull), ph) || !wait_all(bar(s, kTFree), ph ^ 1u) ||
-              !wait_all(bar(s, kKvFull), ph)) {
+              !wait_all(bar(s, kKFull), ph)) {
             ok = false;
             break;
           }
@@ -378,7 +432,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       } else {
         for (int li = 0; li < n_local && ok; ++li) {
           const int s = li % ns;
-          if (!wait_all(bar(s, kPReady), (li / ns) & 1)) {
+          if (!wait_all(bar(s, kPReady), (li / ns) & 1) || !wait_all(bar(s, kVFull), (li / ns) & 1)) {
             ok = false;
             break;
           }
@@ -404,7 +458,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t d_s = tmem + s * p.slot_cols;
         for (int c = 0; c < it.nc; ++c) {
           const uint32_t u = cnt_get(kvc, s);
-          if (!wait_all(bar(s, kTFree), (u & 1u) ^ 1u) || !wait_all(bar(s, kKvFull), u & 1u)) {
+          if (!wait_all(bar(s, kTFree), (u & 1u) ^ 1u) || !wait_all(bar(s, kKFull), u & 1u)) {
             ok = false;
             break;
           }
@@ -414,7 +468,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             mma_commit(bar(s, kSFull));
             if (c == it.nc - 1) mma_commit(bar(s, kQEmpty));
           }
-          if (!wait_all(bar(s, kPReady), u & 1u)) {
+          if (!wait_all(bar(s, kPReady), u & 1u) || !wait_all(bar(s, kVFull), u & 1u)) {
             ok = false;
             break;
           }
@@ -471,13 +525,10 @@ __global__ void __launch_bounds__(kThreads, 1)
       float acc[kMulti ? D : 1];
       for (int c = 0; c < it.nc; ++c) {
         const uint32_t u = kMulti ? cnt_get(kvc, s) : static_cast<uint32_t>(li / ns);
-        if (!wait_all(bar(s, kSFull), u & 1u)) {
-          ok = false;
-          break;
-        }
-        fence_after_sync();
-        // this row's columns [a, e) of the chunk; the warp's union, in
-        // 16-column pieces [w0, w1)
+        // this row's columns [a, e) of the chunk, the warp's union in 32-column
+        // pieces [w0, w1) (a piece past N reads columns inside the slot and
+        // masks them) and the fast-path test below depend only on the block
+        // arithmetic: they are settled before the scores are waited for
         const long long kc = static_cast<long long>(it.kb) + static_cast<long long>(c) * N;
         int a = static_cast<int>(max(0LL, min(static_cast<long long>(N), lo - kc)));
         int e = static_cast<int>(max(0LL, min(static_cast<long long>(N), hi - kc)));
@@ -485,17 +536,61 @@ __global__ void __launch_bounds__(kThreads, 1)
           a = N;
           e = 0;
         }
-        // the warp's union in 32-column pieces [w0, w1); a piece past N reads
-        // columns inside the slot and masks them
         const int w0 = __reduce_min_sync(0xffffffffu, a) >> 5;
         const int w1 = (__reduce_max_sync(0xffffffffu, e) + 31) >> 5;
+        // Fast path: every row of the warp that has keys in this chunk has the
+        // same interval [ua, ue), starting on an 8-column boundary and at most
+        // kFastCols wide (the DiT's own-block layers: one 24-frame block per
+        // quadrant).  The warp then reads exactly those columns once, keeps
+        // them in registers for both passes, and masks only a ragged last
+        // 8-column group; rows without keys (padding lanes) compute values
+        // that are never stored.
+        const int ua = __reduce_max_sync(0xffffffffu, a < e ? a : -1);
+        const int ub = __reduce_min_sync(0xffffffffu, a < e ? a : 0x7fffffff);
+        const int ue = __reduce_max_sync(0xffffffffu, a < e ? e : -1);
+        const int uf = __reduce_min_sync(0xffffffffu, a < e ? e : 0x7fffffff);
+        const bool fast = !kMulti && pos_scale && ua >= 0 && ua == ub && ue == uf &&
+                          (ua & 7) == 0 && ue - ua <= kFastCols;
+        if (!wait_all(bar(s, kSFull), u & 1u)) {
+          ok = false;
+          break;
+        }
+        fence_after_sync();
+        const int ng = fast ? (ue - ua + 7) >> 3 : 0;   // 8-column groups
+        uint32_t rw[kFastCols];
         float mx = -INFINITY;
-#pragma unroll 1
-        for (int pc = w0; pc < w1; ++pc) {
-          uint32_t r[32];
-          tmem_ld32(lane_base + col_s + pc * 32, r);
+        if (fast) {
+#pragma unroll
+          for (int g8 = 0; g8 < kFastCols / 8; ++g8)
+            if (g8 < ng) tmem_ld8(lane_base + col_s + ua + g8 * 8, &rw[8 * g8]);
           tmem_wait_ld();
-          mx = max32(r, pc * 32, a, e, pos_scale, sl2, mx);
+          if ((ue - ua) & 7) {   // keys past the interval in the last group
+#pragma unroll
+            for (int j = 0; j < kFastCols; ++j)
+              if (j >= ue - ua) rw[j] = __float_as_uint(-INFINITY);
+          }
+          float mg[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+          for (int g8 = 0; g8 < kFastCols / 8; ++g8) {
+            if (g8 < ng) {
+              const uint32_t *v = &rw[8 * g8];
+              const float m3 = fmax3(fmax3(__uint_as_float(v[0]), __uint_as_float(v[1]),
+                                           __uint_as_float(v[2])),
+                                     fmax3(__uint_as_float(v[3]), __uint_as_float(v[4]),
+                                           __uint_as_float(v[5])),
+                                     fmaxf(__uint_as_float(v[6]), __uint_as_float(v[7])));
+              mg[g8 & 1] = fmaxf(mg[g8 & 1], m3);
+            }
+          }
+          mx = fmaxf(mg[0], mg[1]) * sl2;
+        } else {
+#pragma unroll 1
+          for (int pc = w0; pc < w1; ++pc) {
+            uint32_t r[32];
+            tmem_ld32(lane_base + col_s + pc * 32, r);
+            tmem_wait_ld();
+            mx = max32(r, pc * 32, a, e, pos_scale, sl2, mx);
+          }
         }
         const float m_new = fmaxf(m_run, mx);
         const float m_use = m_new == -INFINITY ? 0.f : m_new;
@@ -506,15 +601,61 @@ __global__ void __launch_bounds__(kThreads, 1)
         // the union P is 0 (stored after every read of the union, since those
         // columns may overlap its S columns)
         float lsum = 0.f;
+        if (fast) {
+          // P of the interval's keys over P columns [ua / 2, ua / 2 + 4 ng),
+          // 0 over the rest of [0, N / 2) (after the interval was read)
+          const float2 sl22 = make_float2(sl2, sl2), negm2 = make_float2(negm, negm);
+          float2 s2 = make_float2(0.f, 0.f);
+#pragma unroll
+          for (int g8 = 0; g8 < kFastCols / 8; ++g8) {
+            if (g8 < ng) {
+              uint32_t pk[4];
+#pragma unroll
+              for (int jj = 0; jj < 4; ++jj) {
+                const float2 tt = __ffma2_rn(
+                    make_float2(__uint_as_float(rw[8 * g8 + 2 * jj]),
+                                __uint_as_float(rw[8 * g8 + 2 * jj + 1])),
+                    sl22, negm2);
+                const float2 pp = make_float2(ex2(tt.x), ex2(tt.y));
+                s2 = __fadd2_rn(s2, pp);
+                pk[jj] = pack_bf16x2(pp.x, pp.y);
+              }
+              tmem_st4(lane_base + col_s + (ua >> 1) + 4 * g8, pk);
+            }
+          }
+          lsum = s2.x + s2.y;
+          // zeros over [0, p0) and [p1, N / 2) with the widest stores that
+          // sit on a multiple of their own width (every bound is a multiple
+          // of 4; a TMEM store costs about the same whatever its width)
+          const uint32_t z[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
+          const int p0 = ua >> 1, p1 = (ua >> 1) + 4 * ng;
 #pragma unroll 1
-        for (int pc = w0; pc < w1; ++pc) {
-          uint32_t r[32];
-          tmem_ld32(lane_base + col_s + pc * 32, r);
-          tmem_wait_ld();
-          lsum += put_p32(r, pc * 32, a, e, pos_scale, sl2, mul, negm,
-                          lane_base + col_s + pc * 16);
-        }
-        {
+          for (int part = 0; part < 2; ++part) {
+            int x = part == 0 ? 0 : p1;
+            const int x1 = part == 0 ? p0 : N / 2;
+#pragma unroll 1
+            while (x < x1) {
+              if ((x & 15) == 0 && x + 16 <= x1) {
+                tmem_st16(lane_base + col_s + x, z);
+                x += 16;
+              } else if ((x & 7) == 0 && x + 8 <= x1) {
+                tmem_st8(lane_base + col_s + x, z);
+                x += 8;
+              } else {
+                tmem_st4(lane_base + col_s + x, z);
+                x += 4;
+              }
+            }
+          }
+        } else {
+#pragma unroll 1
+          for (int pc = w0; pc < w1; ++pc) {
+            uint32_t r[32];
+            tmem_ld32(lane_base + col_s + pc * 32, r);
+            tmem_wait_ld();
+            lsum += put_p32(r, pc * 32, a, e, pos_scale, sl2, mul, negm,
+                            lane_base + col_s + pc * 16);
+          }
           const uint32_t z[16] = {0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u, 0u};
 #pragma unroll 1
           for (int pc = 0; pc < (N + 31) / 32; ++pc)
