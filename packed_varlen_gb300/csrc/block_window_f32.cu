@@ -19,14 +19,17 @@
 // FMAs.  D = 128: kSplit = 2, kRL = 1, 16 rows a task.  A lane keeps its q
 // slices and output accumulators in registers.  The window's keys are the
 // same for the whole warp, so every K or V load is a broadcast of kSplit
-// adjacent 16-byte words.  The online softmax runs per lane and row;
-// log2(kSplit) shuffles finish a score.  K/V stages hold 12 keys for D = 64
-// (24- and 72-key windows fill them exactly) and 16 for D = 128.
+// adjacent 16-byte words.  The online softmax runs per lane and row, one
+// update per stage of keys (D = 64: 12 keys, so a 24-key window takes two
+// updates; D = 128: 8); log2(kSplit) shuffles finish a score.  K/V stages
+// hold 12 keys for D = 64 (24- and 72-key windows fill them exactly) and 16
+// for D = 128.
 //
 // Pipeline.  Every warp is its own pipeline: it owns a run of consecutive
 // tasks and streams, for each, the task's q rows and then its window in
 // kStage-key K/V stages through a private kBuf-slot shared-memory ring filled
-// by cp.async, so the next stages (and the next task's q) arrive while the
+// by cp.async (four slots for D = 64, three for D = 128: two CTAs per SM
+// either way), so the next stages (and the next task's q) arrive while the
 // current one computes.  Warps never wait for one another.  q is stored with
 // its 16-byte chunks XOR-swizzled by row, so the lanes' reads of their own
 // rows hit distinct banks.
@@ -40,7 +43,6 @@ namespace {
 
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
-constexpr int kBuf = 3;       // ring slots per warp
 
 struct BwF32Params {
   const float *q, *k, *v;
@@ -118,15 +120,16 @@ struct F32Shape {
   static constexpr int kSplit = D == 64 ? 4 : 2;    // lanes per row group
   static constexpr int kRL = D == 64 ? 3 : 1;       // rows per lane
   static constexpr int kRows = 32 / kSplit * kRL;   // rows per warp task
-  static constexpr int kGroup = D == 64 ? 4 : 8;    // keys per online-softmax update
+  static constexpr int kGroup = D == 64 ? 12 : 8;   // keys per online-softmax update
   static constexpr int kStage = D == 64 ? 12 : 16;  // keys per K/V stage (whole groups)
+  static constexpr int kBuf = D == 64 ? 4 : 3;      // ring slots per warp (2 CTAs per SM)
 };
 
 template <int D>
 __global__ void __launch_bounds__(kThreads) block_window_f32_kernel(const BwF32Params p) {
   using S = F32Shape<D>;
   constexpr int kSplit = S::kSplit, kRL = S::kRL, kRows = S::kRows, kGroup = S::kGroup;
-  constexpr int kStage = S::kStage;
+  constexpr int kStage = S::kStage, kBuf = S::kBuf;
   constexpr int kD4 = D / 4;                  // float4 per row
   constexpr int kF4 = kD4 / kSplit;           // float4 slots per lane and row
   constexpr int kSlot = 2 * kStage * D;       // floats per ring slot: K and V of a stage
@@ -321,7 +324,7 @@ bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) ==
 template <int D>
 cudaError_t launch_f32(BwF32Params p, int batch, int H, cudaStream_t st) {
   constexpr int kRows = F32Shape<D>::kRows;
-  constexpr int kSmem = kWarps * kBuf * 2 * F32Shape<D>::kStage * D * 4;
+  constexpr int kSmem = kWarps * F32Shape<D>::kBuf * 2 * F32Shape<D>::kStage * D * 4;
   static unsigned long long done = 0;
   cudaError_t e = set_smem_once(reinterpret_cast<const void *>(&block_window_f32_kernel<D>),
                                 kSmem, done);
