@@ -132,7 +132,10 @@ pa_status pa_block_window_attn_fwd(const void *q, const void *k, const void *v, 
  * contiguous, 16-byte aligned, caller-owned; out must not overlap q, k or v.
  * Every product and sum is IEEE fp32 (no tensor-core tf32); the softmax runs
  * in base 2 on the hardware exp2 with scale * log2(e) folded into q, so the
- * result is within a few fp32 roundings of the exact one.
+ * result is within a few fp32 roundings of the exact one.  Rows are staged
+ * with TMA tensor copies (strides H * D * 4 and n * H * D * 4 bytes, so the
+ * 16-byte alignment above is what they need); a wait that runs out records
+ * PA_DEVICE_ERR_TIMEOUT in the device status word.
  */
 pa_status pa_block_window_attn_fwd_f32(const float *q, const float *k, const float *v,
                                        float *out, int32_t batch, int32_t n, int32_t block,

@@ -27,16 +27,24 @@
 //
 // Pipeline.  Every warp is its own pipeline: it owns a run of consecutive
 // tasks and streams, for each, the task's q rows and then its window in
-// kStage-key K/V stages through a private kBuf-slot shared-memory ring filled
-// by cp.async (four slots for D = 64, three for D = 128: two CTAs per SM
-// either way), so the next stages (and the next task's q) arrive while the
-// current one computes.  Warps never wait for one another.  q is stored with
-// its 16-byte chunks XOR-swizzled by row, so the lanes' reads of their own
-// rows hit distinct banks.
+// kStage-key K/V stages through a private kBuf-slot shared-memory ring (four
+// slots for D = 64, three for D = 128: two CTAs per SM either way), so the
+// next stages (and the next task's q) arrive while the current one computes.
+// One lane issues each stage as TMA tensor copies (one box of q rows, or one
+// box each of K and V rows) completing on the slot's mbarrier: a layer's
+// loads are DRAM-bound, and per-thread 16-byte copies of these 256-byte rows
+// (4 KB apart) reach only ~3.5 TB/s.  Rows outside [0, n) read as zero; V
+// rows past the window in a partial last stage are cleared before use, so
+// keys outside a window contribute nothing whatever their bits.  Warps never
+// wait for one another.
+#include <cuda.h>
 #include <math.h>
 #include <stdint.h>
 
 #include "internal.h"
+#include "sched.cuh"
+#include "tc_ptx.cuh"
+#include "tma_map.h"
 
 namespace pa {
 namespace {
@@ -45,7 +53,6 @@ constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 
 struct BwF32Params {
-  const float *q, *k, *v;
   float *out;
   int64_t row_stride;   // H * D
   float q_scale;        // scale * log2(e)
@@ -54,13 +61,28 @@ struct BwF32Params {
   int64_t tasks_per_row;   // tasks of one (batch entry, head)
   int64_t n_tasks;         // over all batch entries and heads
   int tasks_per_warp;
+  int32_t *status;
 };
 
-// One warp task: rows [row_lo, row_hi) of one (batch entry, head) and their
-// key window [lo, hi); `off` is the element offset of (entry, row 0, head).
+constexpr long long kWaitLimit = 4000000000LL;   // clock cycles (~2 s)
+constexpr long long kDrainLimit = 400000000LL;   // teardown after an abort (~0.2 s)
+
+// 4-D tiled load (coordinates innermost first) completing on `bar`.
+__device__ __forceinline__ void tma_load_4d_f32(uint32_t dst, const CUtensorMap *map,
+                                                uint32_t bar, int c0, int c1, int c2, int c3) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes "
+      "[%0], [%1, {%3, %4, %5, %6}], [%2];\n" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+
+// One warp task: rows [row_lo, row_hi) of batch entry `seq`, head `h`, and
+// their key window [lo, hi); `off` is the element offset of (entry, row 0,
+// head).
 struct Task {
   int64_t off;
-  int row_lo, row_hi, lo, hi;
+  int seq, h, row_lo, row_hi, lo, hi;
 };
 
 template <int D>
@@ -81,6 +103,8 @@ __device__ __forceinline__ Task task_of(const BwF32Params &p, int64_t T) {
   const int64_t hh = (b + 1 + p.look_ahead) * p.block;
   Task k;
   k.off = seq * p.n * p.row_stride + h * D;
+  k.seq = static_cast<int>(seq);
+  k.h = static_cast<int>(h);
   k.row_lo = static_cast<int>(first);
   k.row_hi = static_cast<int>(last);
   k.lo = static_cast<int>(l > 0 ? l : 0);
@@ -93,19 +117,6 @@ __device__ __forceinline__ int kv_stages(const Task &k) {
   return (k.hi - k.lo + kStage - 1) / kStage;
 }
 
-__device__ __forceinline__ void cp_async16(float *smem_dst, const float *src, bool valid) {
-  const uint32_t dst = static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst));
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;\n" ::"r"(dst), "l"(src),
-               "r"(valid ? 16 : 0)
-               : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() {
-  asm volatile("cp.async.commit_group;\n" ::: "memory");
-}
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-  asm volatile("cp.async.wait_group %0;\n" ::"n"(N) : "memory");
-}
 __device__ __forceinline__ float exp2_hw(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;\n" : "=f"(y) : "f"(x));
@@ -126,7 +137,10 @@ struct F32Shape {
 };
 
 template <int D>
-__global__ void __launch_bounds__(kThreads) block_window_f32_kernel(const BwF32Params p) {
+__global__ void __launch_bounds__(kThreads)
+    block_window_f32_kernel(const __grid_constant__ CUtensorMap tm_q,
+                            const __grid_constant__ CUtensorMap tm_k,
+                            const __grid_constant__ CUtensorMap tm_v, const BwF32Params p) {
   using S = F32Shape<D>;
   constexpr int kSplit = S::kSplit, kRL = S::kRL, kRows = S::kRows, kGroup = S::kGroup;
   constexpr int kStage = S::kStage, kBuf = S::kBuf;
@@ -135,52 +149,61 @@ __global__ void __launch_bounds__(kThreads) block_window_f32_kernel(const BwF32P
   constexpr int kSlot = 2 * kStage * D;       // floats per ring slot: K and V of a stage
   static_assert(kRows * D <= kSlot, "a slot holds a task's q rows");
   static_assert(kStage % kGroup == 0, "stages hold whole groups");
-  constexpr int kSwzP = 8 / kSplit;           // row groups per swizzle period
-  extern __shared__ __align__(16) float smem[];
+  extern __shared__ __align__(128) float smem[];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   float *ring = smem + warp * kBuf * kSlot;
+  // per warp kBuf mbarriers after all rings, then the CTA's abort flag
+  const uint32_t bars = tc::smem_u32(smem + kWarps * kBuf * kSlot) + 8u * warp * kBuf;
+  volatile int32_t *abort_flag =
+      reinterpret_cast<volatile int32_t *>(smem + kWarps * kBuf * kSlot + 2 * kWarps * kBuf);
+  if (lane == 0) {
+    for (int b = 0; b < kBuf; ++b) tc::mbar_init(bars + 8u * b, 1);
+    tc::fence_mbar_init();
+  }
+  if (threadIdx.x == 0) {
+    *abort_flag = 0;
+    tc::tma_prefetch_desc(&tm_q);
+    tc::tma_prefetch_desc(&tm_k);
+    tc::tma_prefetch_desc(&tm_v);
+  }
+  __syncthreads();
   const int64_t gw = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
   const int64_t t_begin = gw * p.tasks_per_warp;
   int64_t t_end = t_begin + p.tasks_per_warp;
   if (t_end > p.n_tasks) t_end = p.n_tasks;
   if (t_begin >= t_end) return;   // warps share nothing: an idle warp may leave
 
-  // q chunk c of task row r sits at chunk c ^ swz(r): the lanes reading one
-  // chunk of their rows hit distinct banks
-  auto swz = [](int r) { return ((r / kRL) % kSwzP) * kSplit; };
-
   // ---- producer cursor: stage `is` of task `it` (0: q rows, 1..: K/V) ----
   int64_t it = t_begin;
   int is = 0;
   Task ti = task_of<kRows, D>(p, it);
   int slot_in = 0;
+  uint32_t issued = 0;   // stages issued by this warp
   auto issue_next = [&]() {
     if (it < t_end) {
-      float *dst = ring + slot_in * kSlot;
-      if (is == 0) {
-        for (int idx = lane; idx < kRows * kD4; idx += 32) {
-          const int r = idx / kD4, c = idx % kD4;
-          const bool ok = ti.row_lo + r < ti.row_hi;
-          cp_async16(dst + r * D + 4 * (c ^ swz(r)),
-                     p.q + (ok ? ti.off + (ti.row_lo + r) * p.row_stride + 4 * c : 0), ok);
-        }
-      } else {
-        const int kt = ti.lo + (is - 1) * kStage;
-        for (int idx = lane; idx < kStage * kD4; idx += 32) {
-          const int j = idx / kD4, c = idx % kD4;
-          const bool ok = kt + j < ti.hi;
-          const int64_t src = ok ? ti.off + (kt + j) * p.row_stride + 4 * c : 0;
-          cp_async16(dst + j * D + 4 * c, p.k + src, ok);
-          cp_async16(dst + kStage * D + j * D + 4 * c, p.v + src, ok);
+      const uint32_t dst = tc::smem_u32(ring + slot_in * kSlot);
+      const uint32_t bar = bars + 8u * slot_in;
+      if (lane == 0) {
+        // the warp's earlier reads of this slot (ordered by the __syncwarp
+        // that ends every round) come before the copy's writes
+        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        if (is == 0) {
+          tc::mbar_arrive_expect_tx(bar, kRows * D * 4);
+          tma_load_4d_f32(dst, &tm_q, bar, 0, ti.h, ti.row_lo, ti.seq);
+        } else {
+          const int kt = ti.lo + (is - 1) * kStage;
+          tc::mbar_arrive_expect_tx(bar, 2 * kStage * D * 4);
+          tma_load_4d_f32(dst, &tm_k, bar, 0, ti.h, kt, ti.seq);
+          tma_load_4d_f32(dst + kStage * D * 4, &tm_v, bar, 0, ti.h, kt, ti.seq);
         }
       }
+      ++issued;
       if (++is > kv_stages<kStage>(ti)) {
         is = 0;
         if (++it < t_end) ti = task_of<kRows, D>(p, it);
       }
     }
-    cp_async_commit();   // an empty group past the end keeps the count uniform
     slot_in = slot_in + 1 == kBuf ? 0 : slot_in + 1;
   };
 #pragma unroll
@@ -191,13 +214,21 @@ __global__ void __launch_bounds__(kThreads) block_window_f32_kernel(const BwF32P
   const int r0 = (lane / kSplit) * kRL;   // this lane's first task row
   float2 q2[kRL][2 * kF4], acc2[kRL][2 * kF4];
   float m[kRL], l[kRL];
-  Task tc{0, 0, 0, 0, 0};
+  Task tc{0, 0, 0, 0, 0, 0, 0};
   int cs = 0, n_kv = 0, slot = 0;
+  uint32_t consumed = 0;   // stages consumed by this warp
+  bool ok = true;
   for (int64_t ct = t_begin; ct < t_end;) {
-    cp_async_wait<kBuf - 2>();
-    __syncwarp();          // the slot's copies from every lane are visible
+    // the stage's copies have landed (phase of the slot's consumed-th use)
+    const bool w = tc::bounded_wait(bars + 8u * slot, (consumed / kBuf) & 1u, abort_flag,
+                                    p.status, kWaitLimit);
+    if (!__all_sync(0xffffffffu, w)) {
+      ok = false;
+      break;
+    }
+    ++consumed;
     issue_next();          // refills the slot consumed last round
-    const float *cur = ring + slot * kSlot;
+    float *cur = ring + slot * kSlot;
     if (cs == 0) {
       tc = task_of<kRows, D>(p, ct);
       n_kv = kv_stages<kStage>(tc);
@@ -207,7 +238,7 @@ __global__ void __launch_bounds__(kThreads) block_window_f32_kernel(const BwF32P
         const float4 *qr = reinterpret_cast<const float4 *>(cur + (r0 + rr) * D);
 #pragma unroll
         for (int i = 0; i < kF4; ++i) {
-          const float4 x = qr[(i * kSplit + part) ^ swz(r0 + rr)];
+          const float4 x = qr[i * kSplit + part];
           q2[rr][2 * i] = __fmul2_rn(make_float2(x.x, x.y), s2);
           q2[rr][2 * i + 1] = __fmul2_rn(make_float2(x.z, x.w), s2);
         }
@@ -219,6 +250,14 @@ __global__ void __launch_bounds__(kThreads) block_window_f32_kernel(const BwF32P
     } else {
       const int kt = tc.lo + (cs - 1) * kStage;
       const int e = tc.hi < kt + kStage ? tc.hi : kt + kStage;
+      if (e < kt + kStage) {
+        // a partial last stage: the copy brought rows past the window (or
+        // zeros past n); P is 0 there, but 0 * Inf and 0 * NaN are NaN
+        float4 *vz = reinterpret_cast<float4 *>(cur + kStage * D);
+        for (int idx = (e - kt) * kD4 + lane; idx < kStage * kD4; idx += 32)
+          vz[idx] = make_float4(0.f, 0.f, 0.f, 0.f);
+        __syncwarp();
+      }
       const float4 *k4 = reinterpret_cast<const float4 *>(cur) + part;
       const float4 *v4 = reinterpret_cast<const float4 *>(cur + kStage * D) + part;
 #pragma unroll
@@ -316,25 +355,54 @@ __global__ void __launch_bounds__(kThreads) block_window_f32_kernel(const BwF32P
       ++cs;
     }
   }
-  cp_async_wait<0>();   // nothing in flight at exit
+  if (!ok) {
+    // give the copies already issued a bounded chance to land
+    for (uint32_t u = consumed; u < issued; ++u)
+      tc::drain_wait(bars + 8u * (u % kBuf), (u / kBuf) & 1u, kDrainLimit);
+  }
 }
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// fp32 [batch, n, H, D] as a 4-D tensor (D, H, n, batch); box D x 1 x rows
+// x 1, no swizzle: `rows` consecutive tokens of one head.  Rows outside
+// [0, n) of an entry read as zero.
+bool make_map_f32(CUtensorMap *map, const float *ptr, int batch, int n, int H, int D, int rows) {
+  EncodeTiledFn enc = tensor_map_encoder();
+  if (enc == nullptr) return false;
+  const cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
+                              static_cast<cuuint64_t>(n), static_cast<cuuint64_t>(batch)};
+  const cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 4,
+                                 static_cast<cuuint64_t>(H) * D * 4,
+                                 static_cast<cuuint64_t>(n) * H * D * 4};
+  const cuuint32_t box[4] = {static_cast<cuuint32_t>(D), 1, static_cast<cuuint32_t>(rows), 1};
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, const_cast<float *>(ptr), dims, strides,
+             box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int D>
-cudaError_t launch_f32(BwF32Params p, int batch, int H, cudaStream_t st) {
-  constexpr int kRows = F32Shape<D>::kRows;
-  constexpr int kSmem = kWarps * F32Shape<D>::kBuf * 2 * F32Shape<D>::kStage * D * 4;
+cudaError_t launch_f32(BwF32Params p, const float *q, const float *k, const float *v, int batch,
+                       int H, int sms, cudaStream_t st) {
+  using S = F32Shape<D>;
+  constexpr int kRows = S::kRows;
+  // rings, then kBuf mbarriers per warp, then the abort flag
+  constexpr int kSmem = kWarps * S::kBuf * 2 * S::kStage * D * 4 + kWarps * S::kBuf * 8 + 16;
+  CUtensorMap mq, mk, mv;
+  if (!make_map_f32(&mq, q, batch, p.n, H, D, kRows) ||
+      !make_map_f32(&mk, k, batch, p.n, H, D, S::kStage) ||
+      !make_map_f32(&mv, v, batch, p.n, H, D, S::kStage))
+    return cudaErrorInvalidValue;
   static unsigned long long done = 0;
   cudaError_t e = set_smem_once(reinterpret_cast<const void *>(&block_window_f32_kernel<D>),
                                 kSmem, done);
   if (e != cudaSuccess) return e;
   // resident CTAs per SM, per device (a benign race: every writer stores the same value)
   static int resident[64];
-  int dev = 0, sms = 0;
+  int dev = 0;
   if ((e = cudaGetDevice(&dev)) != cudaSuccess) return e;
-  if ((e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev)) != cudaSuccess)
-    return e;
   int per_sm = resident[dev & 63];
   if (per_sm == 0) {
     if ((e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, block_window_f32_kernel<D>,
@@ -353,7 +421,7 @@ cudaError_t launch_f32(BwF32Params p, int batch, int H, cudaStream_t st) {
   if (tpw > 0x7fffffff) return cudaErrorInvalidConfiguration;
   p.tasks_per_warp = static_cast<int>(tpw);
   const int64_t ctas = (p.n_tasks + tpw * kWarps - 1) / (tpw * kWarps);
-  block_window_f32_kernel<D><<<static_cast<unsigned>(ctas), kThreads, kSmem, st>>>(p);
+  block_window_f32_kernel<D><<<static_cast<unsigned>(ctas), kThreads, kSmem, st>>>(mq, mk, mv, p);
   return cudaGetLastError();
 }
 
@@ -375,8 +443,13 @@ extern "C" pa_status pa_block_window_attn_fwd_f32(const float *q, const float *k
     return PA_ERR_MISALIGNED;
   const float q_scale = static_cast<float>(static_cast<double>(scale) * 1.4426950408889634);
   if (!isfinite(q_scale)) return PA_ERR_INVALID_ARG;
-  BwF32Params p{q, k, v, out, static_cast<int64_t>(H) * D, q_scale, n, block, look_back,
-                look_ahead, H, 0, 0, 0};
+  int32_t *status;
+  int sms;
+  cudaError_t e = device_context(&status, &sms);
+  if (e != cudaSuccess) return from_cuda(e);
+  BwF32Params p{out, static_cast<int64_t>(H) * D, q_scale, n, block, look_back, look_ahead,
+                H, 0, 0, 0, status};
   auto st = reinterpret_cast<cudaStream_t>(stream);
-  return from_cuda(D == 64 ? launch_f32<64>(p, batch, H, st) : launch_f32<128>(p, batch, H, st));
+  return from_cuda(D == 64 ? launch_f32<64>(p, q, k, v, batch, H, sms, st)
+                           : launch_f32<128>(p, q, k, v, batch, H, sms, st));
 }
