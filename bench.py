@@ -105,7 +105,8 @@ def _kernel_digest() -> str:
     to the code it was taken on)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "packed_varlen_gb300", "csrc")
-    for name in ("attn_pair.cu", "tc_ptx.cuh", "sched.cuh", "internal.h", "tma_map.h"):
+    for name in ("attn_pair.cu", "varlen_items.cuh", "tc_ptx.cuh", "sched.cuh", "internal.h",
+                 "tma_map.h"):
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode())
             h.update(f.read())

@@ -46,6 +46,7 @@
 #include "sched.cuh"
 #include "tc_ptx.cuh"
 #include "tma_map.h"
+#include "varlen_items.cuh"
 
 namespace pa {
 namespace {
@@ -53,8 +54,8 @@ namespace {
 using namespace tc;
 
 constexpr int kD = 128;
-constexpr int kTile = 128;          // query rows per CTA, keys per key tile
-constexpr int kItemRows = 256;      // query rows per work item (one pair)
+constexpr int kTile = kVarlenTile;          // query rows per CTA, keys per key tile
+constexpr int kItemRows = kVarlenItemRows;  // query rows per work item (one pair)
 constexpr int kCluster = 2;
 constexpr int kSBufs = 3;           // S/P buffers in TMEM
 constexpr int kThreads = 320;       // producer, MMA issuer, 8 softmax warps
@@ -100,51 +101,6 @@ struct PairCfg {
   static constexpr uint32_t kIdescO = idesc_bf16_f32(kCluster * kTile, kD, true);
 };
 
-struct PairParams {
-  __nv_bfloat16 *out;
-  const int32_t *cu_q, *cu_k;
-  int batch, H, total_q, total_k, max_q, max_k;
-  float scale_log2;
-  int32_t *status;
-};
-
-struct ItemInfo {
-  int q_row0;   // global row of the item's first query
-  int rows;     // valid query rows in the item (1..256)
-  int k0;       // global row of the sequence's first key
-  int lk;       // keys of the sequence
-  int nk;       // key tiles
-  int head;
-  int rot;      // first key tile visited
-};
-
-// Key tile visited j-th: items start at key tile (item index in the sequence
-// mod nk) and wrap around, so the pairs of a wave, which hold consecutive
-// query blocks of one head, read different K/V tiles at any moment.  The
-// order depends only on the sequence's own lengths and the item's position
-// in it, so a sequence's result is the same in any batch.
-__device__ __forceinline__ int key_tile(const ItemInfo &it, int j) {
-  const int kt = it.rot + j;
-  return kt >= it.nk ? kt - it.nk : kt;
-}
-
-__device__ __forceinline__ ItemInfo item_info(const PairParams &p, const int32_t *order,
-                                              const int32_t *prefix, int i) {
-  const WorkItem w = sched_item(order, prefix, p.batch, p.H, i);
-  int err;
-  const SeqBounds sb = seq_bounds(p.cu_q, p.cu_k, w.seq, p.total_q, p.total_k, p.max_q,
-                                  p.max_k, err);
-  ItemInfo it;
-  it.q_row0 = sb.q0 + w.tile * kItemRows;
-  it.rows = min(kItemRows, sb.lq - w.tile * kItemRows);
-  it.k0 = sb.k0;
-  it.lk = sb.lk;
-  it.nk = (sb.lk + kTile - 1) / kTile;
-  it.head = w.head;
-  it.rot = it.nk > 0 ? w.tile % it.nk : 0;
-  return it;
-}
-
 // A position in a pair's stream of key tiles: items i0, i0 + stride, ...,
 // skipping items without keys; tile j of item i.  done() once past the end.
 struct Walk {
@@ -152,7 +108,7 @@ struct Walk {
   ItemInfo it;
   __device__ __forceinline__ bool done() const { return i >= n_items; }
 };
-__device__ __forceinline__ void walk_seek(Walk &w, const PairParams &p, const int32_t *order,
+__device__ __forceinline__ void walk_seek(Walk &w, const VarlenParams &p, const int32_t *order,
                                           const int32_t *prefix) {
   w.j = 0;
   while (w.i < w.n_items) {
@@ -161,7 +117,7 @@ __device__ __forceinline__ void walk_seek(Walk &w, const PairParams &p, const in
     w.i += w.stride;
   }
 }
-__device__ __forceinline__ void walk_next(Walk &w, const PairParams &p, const int32_t *order,
+__device__ __forceinline__ void walk_next(Walk &w, const VarlenParams &p, const int32_t *order,
                                           const int32_t *prefix) {
   if (++w.j < w.it.nk) return;
   w.i += w.stride;
@@ -231,7 +187,7 @@ __device__ __forceinline__ void tile_p(uint32_t taddr, int valid, float sl2, flo
 __global__ void __cluster_dims__(kCluster, 1, 1) __launch_bounds__(kThreads, 1)
     varlen_attn_pair_kernel(const __grid_constant__ CUtensorMap tm_q,
                             const __grid_constant__ CUtensorMap tm_k,
-                            const __grid_constant__ CUtensorMap tm_v, const PairParams p) {
+                            const __grid_constant__ CUtensorMap tm_v, const VarlenParams p) {
   using C = PairCfg;
   extern __shared__ uint8_t smem_raw[];
   // 128-byte swizzle atoms need a 1024-byte aligned base.  Both CTAs of a
@@ -736,7 +692,7 @@ cudaError_t launch_varlen_attn_pair(const VarlenArgs &a, cudaStream_t stream) {
       !make_map_rows(&mk, a.k, a.total_k, a.H, 64) ||
       !make_map_rows(&mv, a.v, a.total_k, a.H, kTile))
     return cudaErrorInvalidValue;
-  PairParams p;
+  VarlenParams p;
   p.out = static_cast<__nv_bfloat16 *>(a.out);
   p.cu_q = a.cu_q;
   p.cu_k = a.cu_k;

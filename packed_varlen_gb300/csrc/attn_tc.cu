@@ -49,14 +49,15 @@
 #include "sched.cuh"
 #include "tc_ptx.cuh"
 #include "tma_map.h"
+#include "varlen_items.cuh"
 
 namespace pa {
 namespace {
 
 using namespace tc;
 
-constexpr int kTile = 128;          // rows of a Q tile, keys of a K/V tile
-constexpr int kItemRows = 256;      // query rows per work item (two tiles)
+constexpr int kTile = kVarlenTile;          // rows of a Q tile, keys of a K/V tile
+constexpr int kItemRows = kVarlenItemRows;  // query rows per work item (two tiles)
 constexpr int kThreads = 352;       // producer, 2 MMA issuers, 2 x 4 softmax warps
 constexpr int kMmaWarp1 = kThreads / 32 - 1;   // issuer of tile 1
 constexpr long long kWaitLimit = 4000000000LL;  // clock cycles (~2 s)
@@ -94,51 +95,6 @@ struct Cfg {
   static constexpr uint32_t kVLbo = D == 128 ? kHalfBytes : 1024;
 };
 
-struct TcParams {
-  __nv_bfloat16 *out;
-  const int32_t *cu_q, *cu_k;
-  int batch, H, total_q, total_k, max_q, max_k;
-  float scale_log2;
-  int32_t *status;
-};
-
-struct ItemInfo {
-  int q_row0;   // global row of the item's first query
-  int rows;     // valid query rows in the item (1..256)
-  int k0;       // global row of the sequence's first key
-  int lk;       // keys of the sequence
-  int nk;       // key tiles
-  int head;
-  int rot;      // first key tile visited
-};
-
-// Key tile visited j-th.  Items start at key tile (item index in the
-// sequence mod nk) and wrap around, so the CTAs of a wave, which hold
-// consecutive query blocks of one head, read different K/V tiles at any
-// moment.  The order depends only on the sequence's own lengths and the
-// item's position in it, so a sequence's result is the same in any batch.
-__device__ __forceinline__ int key_tile(const ItemInfo &it, int j) {
-  const int kt = it.rot + j;
-  return kt >= it.nk ? kt - it.nk : kt;
-}
-
-__device__ __forceinline__ ItemInfo item_info(const TcParams &p, const int32_t *order,
-                                              const int32_t *prefix, int i) {
-  const WorkItem w = sched_item(order, prefix, p.batch, p.H, i);
-  int err;
-  const SeqBounds sb = seq_bounds(p.cu_q, p.cu_k, w.seq, p.total_q, p.total_k, p.max_q,
-                                  p.max_k, err);
-  ItemInfo it;
-  it.q_row0 = sb.q0 + w.tile * kItemRows;
-  it.rows = min(kItemRows, sb.lq - w.tile * kItemRows);
-  it.k0 = sb.k0;
-  it.lk = sb.lk;
-  it.nk = (sb.lk + kTile - 1) / kTile;
-  it.head = w.head;
-  it.rot = it.nk > 0 ? w.tile % it.nk : 0;
-  return it;
-}
-
 // Whole warp: zero key rows [valid, 128) of a V tile in shared memory.  The
 // tile is D / 64 column halves of 128 rows x 128 bytes; the 128-byte swizzle
 // only permutes the 16-byte chunks inside a row, so a whole row is cleared
@@ -161,7 +117,7 @@ template <int D, int kSlots, int kMaxSeqs>
 __global__ void __launch_bounds__(kThreads, 1)
     varlen_attn_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                           const __grid_constant__ CUtensorMap tm_k,
-                          const __grid_constant__ CUtensorMap tm_v, const TcParams p) {
+                          const __grid_constant__ CUtensorMap tm_v, const VarlenParams p) {
   using C = Cfg<D, kSlots, kMaxSeqs>;
   extern __shared__ uint8_t smem_raw[];
   // 128-byte swizzle atoms need a 1024-byte aligned base
@@ -618,7 +574,7 @@ cudaError_t launch_tc(const VarlenArgs &a, cudaStream_t stream) {
   if (!make_map(&mq, a.q, a.total_q, a.H, D) || !make_map(&mk, a.k, a.total_k, a.H, D) ||
       !make_map(&mv, a.v, a.total_k, a.H, D))
     return cudaErrorInvalidValue;
-  TcParams p;
+  VarlenParams p;
   p.out = static_cast<__nv_bfloat16 *>(a.out);
   p.cu_q = a.cu_q;
   p.cu_k = a.cu_k;

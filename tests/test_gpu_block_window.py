@@ -129,6 +129,23 @@ def test_window_shapes_against_oracle(pv, block, n, look):
     assert pv.get_device_status() == 0
 
 
+@pytest.mark.parametrize("block,n,look,D", [(20, 507, (0, 0), 64), (28, 333, (0, 0), 128),
+                                            (32, 300, (0, 0), 64), (24, 250, (0, 0), 64),
+                                            (20, 507, (1, 0), 64)])
+def test_one_window_path_edges(pv, block, n, look, D):
+    # A warp whose rows share one key interval that starts on an 8-column
+    # boundary and is at most 32 keys wide reads exactly that interval; here
+    # intervals that end inside an 8-column group (20- and 28-frame blocks, a
+    # window clipped at n), that start off an 8-column boundary (so the warp
+    # takes the masked path beside warps that take the exact one), that are
+    # exactly 32 wide, and that are wider than 32 (the masked path only)
+    w = workloads.random_block_window(2, n, 3, D, block, seed=block * 3 + n)
+    got = oracle.to_f64(_run(pv, w, *look))
+    want = oracle.block_window_attention(w.q, w.k, w.v, block, look[0], look[1], w.scale)
+    assert_close_to_oracle(got, want, f"block={block} n={n} look={look} D={D}")
+    assert pv.get_device_status() == 0
+
+
 def test_chained_layers_respect_stream_order(pv):
     # The kernel is launched so that it may start while the previous kernel
     # on the stream drains; its copies and stores must still wait for that
