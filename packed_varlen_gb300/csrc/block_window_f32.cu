@@ -67,16 +67,6 @@ struct BwF32Params {
 constexpr long long kWaitLimit = 4000000000LL;   // clock cycles (~2 s)
 constexpr long long kDrainLimit = 400000000LL;   // teardown after an abort (~0.2 s)
 
-// 4-D tiled load (coordinates innermost first) completing on `bar`.
-__device__ __forceinline__ void tma_load_4d_f32(uint32_t dst, const CUtensorMap *map,
-                                                uint32_t bar, int c0, int c1, int c2, int c3) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%3, %4, %5, %6}], [%2];\n" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-      : "memory");
-}
-
 // One warp task: rows [row_lo, row_hi) of batch entry `seq`, head `h`, and
 // their key window [lo, hi); `off` is the element offset of (entry, row 0,
 // head).
@@ -187,15 +177,15 @@ __global__ void __launch_bounds__(kThreads)
       if (lane == 0) {
         // the warp's earlier reads of this slot (ordered by the __syncwarp
         // that ends every round) come before the copy's writes
-        asm volatile("fence.proxy.async.shared::cta;\n" ::: "memory");
+        tc::fence_proxy_async();
         if (is == 0) {
           tc::mbar_arrive_expect_tx(bar, kRows * D * 4);
-          tma_load_4d_f32(dst, &tm_q, bar, 0, ti.h, ti.row_lo, ti.seq);
+          tc::tma_load_4d(dst, &tm_q, bar, 0, ti.h, ti.row_lo, ti.seq);
         } else {
           const int kt = ti.lo + (is - 1) * kStage;
           tc::mbar_arrive_expect_tx(bar, 2 * kStage * D * 4);
-          tma_load_4d_f32(dst, &tm_k, bar, 0, ti.h, kt, ti.seq);
-          tma_load_4d_f32(dst + kStage * D * 4, &tm_v, bar, 0, ti.h, kt, ti.seq);
+          tc::tma_load_4d(dst, &tm_k, bar, 0, ti.h, kt, ti.seq);
+          tc::tma_load_4d(dst + kStage * D * 4, &tm_v, bar, 0, ti.h, kt, ti.seq);
         }
       }
       ++issued;

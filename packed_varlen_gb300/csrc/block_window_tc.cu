@@ -130,46 +130,6 @@ __device__ __forceinline__ void cnt_add(uint32_t (&c)[kMaxSlots], int s, uint32_
   for (int i = 0; i < kMaxSlots; ++i) c[i] += (i == s) ? v : 0u;
 }
 
-__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap *map, uint32_t bar,
-                                            int c0, int c1, int c2, int c3) {
-  asm volatile(
-      "cp.async.bulk.tensor.4d.shared::cluster.global.mbarrier::complete_tx::bytes "
-      "[%0], [%1, {%3, %4, %5, %6}], [%2];\n" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
-      : "memory");
-}
-
-// registers -> TMEM, 32 lanes x 16 columns.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t *r) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};\n" ::"r"(taddr),
-      "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]),
-      "r"(r[8]), "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]),
-      "r"(r[15])
-      : "memory");
-}
-// TMEM -> registers, 32 lanes x 8 columns; registers -> TMEM, 32 lanes x 8
-// or 4 columns.  Each is used at a column offset that is a multiple of its
-// width.
-__device__ __forceinline__ void tmem_ld8(uint32_t taddr, uint32_t *r) {
-  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n"
-               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
-                 "=r"(r[6]), "=r"(r[7])
-               : "r"(taddr)
-               : "memory");
-}
-__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t *r) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};\n" ::"r"(
-                   taddr),
-               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
-               : "memory");
-}
-__device__ __forceinline__ void tmem_st4(uint32_t taddr, const uint32_t *r) {
-  asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};\n" ::"r"(taddr),
-               "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3])
-               : "memory");
-}
 constexpr int kFastCols = 32;   // widest window of the one-window fast path
 
 // Bounded mbarrier wait: the first poll inline, the polling loop out of
@@ -182,13 +142,6 @@ __device__ __noinline__ bool bw_wait_slow(uint32_t bar, uint32_t parity,
 __device__ __forceinline__ bool bw_wait(uint32_t bar, uint32_t parity,
                                         volatile int32_t *abort_flag, int32_t *status) {
   return mbar_try_wait(bar, parity) || bw_wait_slow(bar, parity, abort_flag, status);
-}
-
-__device__ __forceinline__ void griddep_wait() {
-  asm volatile("griddepcontrol.wait;\n" ::: "memory");
-}
-__device__ __forceinline__ void griddep_launch_dependents() {
-  asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 }
 
 // Softmax pieces of 32 S columns (keys col0 .. col0 + 31 of the chunk).

@@ -109,3 +109,88 @@ def test_repeatable_with_guard_band(pv):
     torch.cuda.synchronize()
     assert (buf[2 * 257 * 4 * 64:] == 7.0).all()
     assert torch.equal(out.cpu().view(torch.int32), a.view(torch.int32))
+
+
+@pytest.mark.parametrize("block,n,look", [(24, 2400, (1, 0)), (20, 507, (0, 0)), (32, 300, (0, 0)),
+                                          (16, 300, (1, 1)), (8, 250, (0, 0)), (40, 333, (0, 0)),
+                                          (48, 500, (0, 0)), (24, 23, (1, 1))])
+def test_block_and_window_shapes(pv, block, n, look):
+    # one neighbour block on one side; blocks of 20 frames (a 24-row task
+    # split over lanes that cover fewer rows), 32, 16 and 8 frames (several
+    # blocks per 32-row span), 40 and 48 frames (tasks of part of a block),
+    # and a sequence shorter than its block with neighbours on both sides
+    w = workloads.random_block_window_f32(2, n, 3, 64, block, seed=block * 5 + n)
+    want = oracle.block_window_attention(w.q, w.k, w.v, block, look[0], look[1], w.scale)
+    _close(_run(pv, w, *look), want, f"block={block} n={n} look={look}")
+    assert pv.get_device_status() == 0
+
+
+@pytest.mark.parametrize("n,look", [(2390, (1, 1)), (101, (0, 0)), (333, (2, 3))])
+def test_batch_entries_do_not_leak(pv, n, look):
+    # entry 1 is all NaN / +-Inf: entry 0 (whose last rows end where entry 1
+    # begins in memory) must equal its run alone bit for bit and the oracle
+    w = workloads.random_block_window_f32(2, n, 2, 64, 24, seed=n)
+    bad = [t.clone() for t in (w.q, w.k, w.v)]
+    vals = torch.tensor([float("nan"), float("inf"), float("-inf")])
+    for t in bad:
+        t[1] = vals.repeat(t[1].numel() // 3 + 1)[:t[1].numel()].view(t[1].shape)
+    w2 = workloads.BlockWindowWorkload("poisoned", 2, n, 2, 64, 24, [look], *bad, w.seed)
+    got = _run(pv, w2, *look)
+    one = workloads.BlockWindowWorkload("alone", 1, n, 2, 64, 24, [look], w.q[:1].contiguous(),
+                                        w.k[:1].contiguous(), w.v[:1].contiguous(), w.seed)
+    assert torch.equal(got[0].view(torch.int32), _run(pv, one, *look)[0].view(torch.int32))
+    want = oracle.block_window_attention(w.q[:1], w.k[:1], w.v[:1], 24, look[0], look[1], w.scale)
+    _close(got[:1], want, f"entry 0 n={n} look={look}")
+    assert pv.get_device_status() == 0
+
+
+def test_chained_layers_respect_stream_order(pv):
+    # Each layer reads the previous layer's output (read after write), and in
+    # the second chain writes over the buffer the previous layer read (write
+    # after read); no host sync between launches.  The result must equal the
+    # same chain with a sync after every launch.
+    w = workloads.token2wav_f32(n=960)
+    q, k, v = w.q.cuda(), w.k.cuda(), w.v.cuda()
+    looks = [(0, 0), (1, 1), (0, 0), (1, 1), (2, 3), (0, 0)]
+
+    def chain(sync):
+        x = q.clone()
+        for lb, la in looks:
+            x = pv.block_window_attn_fwd_f32(x, k, v, w.block, lb, la)
+            if sync:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        return x
+
+    def chain_in_place(sync):
+        a, b = q.clone(), torch.empty_like(q)
+        for lb, la in looks:
+            pv.block_window_attn_fwd_f32(a, k, v, w.block, lb, la, out=b)
+            a, b = b, a
+            if sync:
+                torch.cuda.synchronize()
+        torch.cuda.synchronize()
+        return a
+
+    assert torch.equal(chain(False).view(torch.int32), chain(True).view(torch.int32))
+    assert torch.equal(chain_in_place(False).view(torch.int32),
+                       chain_in_place(True).view(torch.int32))
+    assert pv.get_device_status() == 0
+
+
+def test_graph_replay_matches_eager(pv):
+    # the 22 Token2Wav layers captured in a CUDA graph give the eager launches' bits
+    w = workloads.token2wav_f32(n=480)
+    q, k, v = w.q.cuda(), w.k.cuda(), w.v.cuda()
+    eager = [pv.block_window_attn_fwd_f32(q, k, v, w.block, lb, la) for lb, la in w.layers]
+    outs = [torch.empty_like(q) for _ in w.layers]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=side):
+        for o, (lb, la) in zip(outs, w.layers):
+            pv.block_window_attn_fwd_f32(q, k, v, w.block, lb, la, out=o)
+    graph.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(eager, outs):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
