@@ -202,6 +202,17 @@ __global__ void __launch_bounds__(kThreads)
   // ---- consumer ----
   const int part = lane % kSplit;
   const int r0 = (lane / kSplit) * kRL;   // this lane's first task row
+  // D = 64: the four lanes of a row group reduce their partial scores by
+  // halves (a transposing butterfly), so that each ends with the full scores
+  // of 3 of a group's 12 keys and computes only their exponentials; the
+  // probabilities are then gathered back.  Register kk of a lane holds key
+  // key_of(kk) of the group, an order that differs per lane so that every
+  // exchange moves register j to register j of the partner.
+  constexpr bool kTransposed = kSplit == 4 && kGroup == 12;
+  const int o6 = (part & 1) ? 6 : 0, o3 = (part & 2) ? 3 : 0;
+  auto key_of = [&](int kk) {
+    return (kk < 6 ? o6 : 6 - o6) + (((kk / 3) & 1) ? 3 - o3 : o3) + kk % 3;
+  };
   float2 q2[kRL][2 * kF4], acc2[kRL][2 * kF4];
   float m[kRL], l[kRL];
   Task tc{0, 0, 0, 0, 0, 0, 0};
@@ -254,70 +265,153 @@ __global__ void __launch_bounds__(kThreads)
       for (int g0 = 0; g0 < kStage; g0 += kGroup) {
         const int g = kt + g0;
         if (g >= e) break;   // warp-uniform
-        float2 sc2[kRL][kGroup];
+        if constexpr (kTransposed) {
+          float2 sc2[kRL][kGroup];
 #pragma unroll
-        for (int rr = 0; rr < kRL; ++rr)
+          for (int rr = 0; rr < kRL; ++rr)
 #pragma unroll
-          for (int kk = 0; kk < kGroup; ++kk) sc2[rr][kk] = make_float2(0.f, 0.f);
+            for (int kk = 0; kk < kGroup; ++kk) sc2[rr][kk] = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int i = 0; i < kF4; ++i) {
+          for (int i = 0; i < kF4; ++i) {
 #pragma unroll
-          for (int kk = 0; kk < kGroup; ++kk) {
-            const float4 kv = k4[(g0 + kk) * kD4 + i * kSplit];
+            for (int kk = 0; kk < kGroup; ++kk) {
+              const float4 kv = k4[(g0 + key_of(kk)) * kD4 + i * kSplit];
 #pragma unroll
-            for (int rr = 0; rr < kRL; ++rr) {
-              sc2[rr][kk] = __ffma2_rn(q2[rr][2 * i], make_float2(kv.x, kv.y), sc2[rr][kk]);
-              sc2[rr][kk] = __ffma2_rn(q2[rr][2 * i + 1], make_float2(kv.z, kv.w), sc2[rr][kk]);
+              for (int rr = 0; rr < kRL; ++rr) {
+                sc2[rr][kk] = __ffma2_rn(q2[rr][2 * i], make_float2(kv.x, kv.y), sc2[rr][kk]);
+                sc2[rr][kk] = __ffma2_rn(q2[rr][2 * i + 1], make_float2(kv.z, kv.w), sc2[rr][kk]);
+              }
             }
           }
-        }
-        float pr[kRL][kGroup], alpha[kRL];
-#pragma unroll
-        for (int rr = 0; rr < kRL; ++rr) {
-#pragma unroll
-          for (int kk = 0; kk < kGroup; ++kk) {
-            float x = sc2[rr][kk].x + sc2[rr][kk].y;
-#pragma unroll
-            for (int sh = 1; sh < kSplit; sh <<= 1) x += __shfl_xor_sync(0xffffffffu, x, sh);
-            pr[rr][kk] = g + kk < e ? x : -INFINITY;   // keys past e: zero-filled rows
-          }
-          float mx = pr[rr][0];
-#pragma unroll
-          for (int kk = 1; kk < kGroup; ++kk) mx = fmaxf(mx, pr[rr][kk]);
-          const float m_new = fmaxf(m[rr], mx);       // finite: key g is in the window
-          alpha[rr] = exp2_hw(m[rr] - m_new);         // 0 on the first group
-          m[rr] = m_new;
-          float psum = 0.f;
-#pragma unroll
-          for (int kk = 0; kk < kGroup; ++kk) {
-            pr[rr][kk] = exp2_hw(pr[rr][kk] - m_new);
-            psum += pr[rr][kk];
-          }
-          l[rr] = l[rr] * alpha[rr] + psum;
-        }
-#pragma unroll
-        for (int i = 0; i < kF4; ++i) {
-          float2 lo2[kRL], hi2[kRL];
+          // registers 6-11 go to the lane across bit 0 (where they are
+          // registers 0-5, the same keys), then registers 3-5 across bit 1
+          float p3[kRL][3], alpha[kRL];
 #pragma unroll
           for (int rr = 0; rr < kRL; ++rr) {
-            const float2 al2 = make_float2(alpha[rr], alpha[rr]);
-            lo2[rr] = __fmul2_rn(acc2[rr][2 * i], al2);
-            hi2[rr] = __fmul2_rn(acc2[rr][2 * i + 1], al2);
+            float s6[6], s3[3];
+#pragma unroll
+            for (int j = 0; j < 6; ++j)
+              s6[j] = (sc2[rr][j].x + sc2[rr][j].y) +
+                      __shfl_xor_sync(0xffffffffu, sc2[rr][j + 6].x + sc2[rr][j + 6].y, 1);
+#pragma unroll
+            for (int j = 0; j < 3; ++j) {
+              s3[j] = s6[j] + __shfl_xor_sync(0xffffffffu, s6[j + 3], 2);
+              if (g + key_of(j) >= e) s3[j] = -INFINITY;   // keys past e: zero-filled rows
+            }
+            float mx = tc::fmax3(s3[0], s3[1], s3[2]);
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+            const float m_new = fmaxf(m[rr], mx);   // finite: key g is in the window
+            alpha[rr] = exp2_hw(m[rr] - m_new);     // 0 on the first group
+            m[rr] = m_new;
+#pragma unroll
+            for (int j = 0; j < 3; ++j) p3[rr][j] = exp2_hw(s3[j] - m_new);
+            // this lane's share of the row sum (the four are added at the end)
+            l[rr] = l[rr] * alpha[rr] + (p3[rr][0] + p3[rr][1] + p3[rr][2]);
+          }
+          // every key's probability back into register order
+          float pr[kRL][kGroup];
+#pragma unroll
+          for (int rr = 0; rr < kRL; ++rr) {
+#pragma unroll
+            for (int j = 0; j < 3; ++j) {
+              pr[rr][j] = p3[rr][j];
+              pr[rr][j + 3] = __shfl_xor_sync(0xffffffffu, p3[rr][j], 2);
+            }
+#pragma unroll
+            for (int j = 0; j < 6; ++j) pr[rr][j + 6] = __shfl_xor_sync(0xffffffffu, pr[rr][j], 1);
           }
 #pragma unroll
-          for (int kk = 0; kk < kGroup; ++kk) {
-            const float4 vv = v4[(g0 + kk) * kD4 + i * kSplit];
+          for (int i = 0; i < kF4; ++i) {
+            float2 lo2[kRL], hi2[kRL];
 #pragma unroll
             for (int rr = 0; rr < kRL; ++rr) {
-              const float2 pk = make_float2(pr[rr][kk], pr[rr][kk]);
-              lo2[rr] = __ffma2_rn(pk, make_float2(vv.x, vv.y), lo2[rr]);
-              hi2[rr] = __ffma2_rn(pk, make_float2(vv.z, vv.w), hi2[rr]);
+              const float2 al2 = make_float2(alpha[rr], alpha[rr]);
+              lo2[rr] = __fmul2_rn(acc2[rr][2 * i], al2);
+              hi2[rr] = __fmul2_rn(acc2[rr][2 * i + 1], al2);
+            }
+#pragma unroll
+            for (int kk = 0; kk < kGroup; ++kk) {
+              const float4 vv = v4[(g0 + key_of(kk)) * kD4 + i * kSplit];
+#pragma unroll
+              for (int rr = 0; rr < kRL; ++rr) {
+                const float2 pk = make_float2(pr[rr][kk], pr[rr][kk]);
+                lo2[rr] = __ffma2_rn(pk, make_float2(vv.x, vv.y), lo2[rr]);
+                hi2[rr] = __ffma2_rn(pk, make_float2(vv.z, vv.w), hi2[rr]);
+              }
+            }
+#pragma unroll
+            for (int rr = 0; rr < kRL; ++rr) {
+              acc2[rr][2 * i] = lo2[rr];
+              acc2[rr][2 * i + 1] = hi2[rr];
             }
           }
-#pragma unroll
+        } else {
+          float2 sc2[kRL][kGroup];
+  #pragma unroll
+          for (int rr = 0; rr < kRL; ++rr)
+  #pragma unroll
+            for (int kk = 0; kk < kGroup; ++kk) sc2[rr][kk] = make_float2(0.f, 0.f);
+  #pragma unroll
+          for (int i = 0; i < kF4; ++i) {
+  #pragma unroll
+            for (int kk = 0; kk < kGroup; ++kk) {
+              const float4 kv = k4[(g0 + kk) * kD4 + i * kSplit];
+  #pragma unroll
+              for (int rr = 0; rr < kRL; ++rr) {
+                sc2[rr][kk] = __ffma2_rn(q2[rr][2 * i], make_float2(kv.x, kv.y), sc2[rr][kk]);
+                sc2[rr][kk] = __ffma2_rn(q2[rr][2 * i + 1], make_float2(kv.z, kv.w), sc2[rr][kk]);
+              }
+            }
+          }
+          float pr[kRL][kGroup], alpha[kRL];
+  #pragma unroll
           for (int rr = 0; rr < kRL; ++rr) {
-            acc2[rr][2 * i] = lo2[rr];
-            acc2[rr][2 * i + 1] = hi2[rr];
+  #pragma unroll
+            for (int kk = 0; kk < kGroup; ++kk) {
+              float x = sc2[rr][kk].x + sc2[rr][kk].y;
+  #pragma unroll
+              for (int sh = 1; sh < kSplit; sh <<= 1) x += __shfl_xor_sync(0xffffffffu, x, sh);
+              pr[rr][kk] = g + kk < e ? x : -INFINITY;   // keys past e: zero-filled rows
+            }
+            float mx = pr[rr][0];
+  #pragma unroll
+            for (int kk = 1; kk < kGroup; ++kk) mx = fmaxf(mx, pr[rr][kk]);
+            const float m_new = fmaxf(m[rr], mx);       // finite: key g is in the window
+            alpha[rr] = exp2_hw(m[rr] - m_new);         // 0 on the first group
+            m[rr] = m_new;
+            float psum = 0.f;
+  #pragma unroll
+            for (int kk = 0; kk < kGroup; ++kk) {
+              pr[rr][kk] = exp2_hw(pr[rr][kk] - m_new);
+              psum += pr[rr][kk];
+            }
+            l[rr] = l[rr] * alpha[rr] + psum;
+          }
+  #pragma unroll
+          for (int i = 0; i < kF4; ++i) {
+            float2 lo2[kRL], hi2[kRL];
+  #pragma unroll
+            for (int rr = 0; rr < kRL; ++rr) {
+              const float2 al2 = make_float2(alpha[rr], alpha[rr]);
+              lo2[rr] = __fmul2_rn(acc2[rr][2 * i], al2);
+              hi2[rr] = __fmul2_rn(acc2[rr][2 * i + 1], al2);
+            }
+  #pragma unroll
+            for (int kk = 0; kk < kGroup; ++kk) {
+              const float4 vv = v4[(g0 + kk) * kD4 + i * kSplit];
+  #pragma unroll
+              for (int rr = 0; rr < kRL; ++rr) {
+                const float2 pk = make_float2(pr[rr][kk], pr[rr][kk]);
+                lo2[rr] = __ffma2_rn(pk, make_float2(vv.x, vv.y), lo2[rr]);
+                hi2[rr] = __ffma2_rn(pk, make_float2(vv.z, vv.w), hi2[rr]);
+              }
+            }
+  #pragma unroll
+            for (int rr = 0; rr < kRL; ++rr) {
+              acc2[rr][2 * i] = lo2[rr];
+              acc2[rr][2 * i + 1] = hi2[rr];
+            }
           }
         }
       }
@@ -328,9 +422,14 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
       for (int rr = 0; rr < kRL; ++rr) {
         const int row = tc.row_lo + r0 + rr;
+        float lr = l[rr];
+        if constexpr (kTransposed) {   // each lane summed its own keys
+          lr += __shfl_xor_sync(0xffffffffu, lr, 1);
+          lr += __shfl_xor_sync(0xffffffffu, lr, 2);
+        }
         if (row < tc.row_hi) {
-          // both parts of a row hold the same l: each saw every score
-          const float inv = 1.f / l[rr];   // l > 0: a row always sees its own block
+          // every part of a row holds the same l
+          const float inv = 1.f / lr;   // l > 0: a row always sees its own block
           float4 *dst = reinterpret_cast<float4 *>(p.out + tc.off + row * p.row_stride);
 #pragma unroll
           for (int i = 0; i < kF4; ++i)
