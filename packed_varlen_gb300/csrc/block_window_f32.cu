@@ -19,9 +19,12 @@
 // FMAs.  D = 128: kSplit = 2, kRL = 1, 16 rows a task.  A lane keeps its q
 // slices and output accumulators in registers.  The window's keys are the
 // same for the whole warp, so every K or V load is a broadcast of kSplit
-// adjacent 16-byte words.  The online softmax runs per lane and row, one
-// update per stage of keys (D = 64: 12 keys, so a 24-key window takes two
-// updates; D = 128: 8); log2(kSplit) shuffles finish a score.  K/V stages
+// adjacent 16-byte words.  The online softmax runs per row, one update per
+// stage of keys (D = 64: 12 keys, so a 24-key window takes two updates;
+// D = 128: 8).  D = 128: log2(kSplit) shuffles finish a score in both lanes.
+// D = 64: the row group's lanes reduce their partial scores by halves, so
+// each holds 3 of the 12 scores, exponentiates only those and keeps its
+// share of the row sum; the probabilities are then gathered back.  K/V stages
 // hold 12 keys for D = 64 (24- and 72-key windows fill them exactly) and 16
 // for D = 128.
 //
