@@ -6,8 +6,9 @@
 // optionally rescaled to the positive row's L2 norm (cfg_normalize).
 //
 // HBM bound: one warp per output row (several rows per warp when a row has
-// fewer than 32 sixteen-byte vectors), 16-byte vector loads and stores, fp32
-// arithmetic (one fused multiply-add per element), bf16 round to nearest.
+// fewer than 32 sixteen-byte vectors), 16-byte vector loads and stores with
+// four vectors of each input in flight per lane, fp32 arithmetic (one fused
+// multiply-add per element), bf16 round to nearest.
 #include <cuda_bf16.h>
 #include <math.h>
 #include <stdint.h>
@@ -19,6 +20,7 @@ namespace pa {
 namespace {
 
 constexpr int kThreads = 256;  // 8 warps, one output row each per step
+constexpr int kBatch = 4;      // 16-byte vectors per lane and input in flight
 
 __device__ __forceinline__ void bf16x8_to_f32(const uint4 &u, float (&f)[8]) {
   const uint32_t w[4] = {u.x, u.y, u.z, u.w};
@@ -114,25 +116,40 @@ __global__ void __launch_bounds__(kThreads)
       factor = cc > 0.f ? sqrtf(pp) / sqrtf(cc) : 0.f;
     }
     if (!live) continue;
-    for (int v = gl; v < vecs; v += group) {
-      float a[8];
-      bf16x8_to_f32(__ldg(pr + v), a);
-      float c[8];
-      if (cfg) {
-        float b[8];
-        bf16x8_to_f32(__ldg(nr + v), b);
+    // kBatch vectors of each input per lane loaded before any is combined
+    for (int v0 = gl; v0 < vecs; v0 += group * kBatch) {
+      uint4 ain[kBatch], bin[kBatch];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) c[k] = fmaf(s, a[k] - b[k], b[k]) * factor;
-      } else {
-#pragma unroll
-        for (int k = 0; k < 8; ++k) c[k] = a[k];
+      for (int u = 0; u < kBatch; ++u) {
+        const int v = v0 + group * u;
+        if (v < vecs) {
+          ain[u] = __ldg(pr + v);
+          if (cfg) bin[u] = __ldg(nr + v);
+        }
       }
-      uint4 w;
-      w.x = pack2(c[0], c[1]);
-      w.y = pack2(c[2], c[3]);
-      w.z = pack2(c[4], c[5]);
-      w.w = pack2(c[6], c[7]);
-      orow[v] = w;
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int v = v0 + group * u;
+        if (v >= vecs) break;
+        float a[8];
+        bf16x8_to_f32(ain[u], a);
+        float c[8];
+        if (cfg) {
+          float b[8];
+          bf16x8_to_f32(bin[u], b);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) c[k] = fmaf(s, a[k] - b[k], b[k]) * factor;
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) c[k] = a[k];
+        }
+        uint4 w;
+        w.x = pack2(c[0], c[1]);
+        w.y = pack2(c[2], c[3]);
+        w.z = pack2(c[4], c[5]);
+        w.w = pack2(c[6], c[7]);
+        orow[v] = w;
+      }
     }
   }
 }
