@@ -61,7 +61,8 @@ struct BwF32Params {
   float q_scale;        // scale * log2(e)
   int n, block, look_back, look_ahead;
   int H;
-  int64_t tasks_per_row;   // tasks of one (batch entry, head)
+  int64_t tasks_per_row;   // tasks of one (batch entry, head): n_blocks * segs
+  int n_blocks, segs;      // blocks of a sequence, tasks of a block
   int64_t n_tasks;         // over all batch entries and heads
   int tasks_per_warp;
   int32_t *status;
@@ -81,23 +82,47 @@ struct Task {
 template <int D>
 struct F32Shape;
 
-template <int kRows, int D>
-__device__ __forceinline__ Task task_of(const BwF32Params &p, int64_t T) {
-  const int segs = (p.block + kRows - 1) / kRows;
-  const int64_t rid = T / p.tasks_per_row;          // (batch entry, head)
+// Position of a task in (batch entry, head, block, segment of the block)
+// order.  A warp's tasks are consecutive, so one decode with divisions at
+// the start is followed by increments only.
+struct TaskPos {
+  int seq, h, b, sg;
+};
+
+__device__ __forceinline__ TaskPos task_pos(const BwF32Params &p, int64_t T) {
+  const int64_t rid = T / p.tasks_per_row;           // (batch entry, head)
   const int64_t t = T - rid * p.tasks_per_row;
-  const int64_t seq = rid / p.H, h = rid - seq * p.H;
-  const int64_t b = t / segs;
-  const int64_t first = b * p.block + (t - b * segs) * kRows;
+  TaskPos c;
+  c.seq = static_cast<int>(rid / p.H);
+  c.h = static_cast<int>(rid - static_cast<int64_t>(c.seq) * p.H);
+  c.b = static_cast<int>(t / p.segs);
+  c.sg = static_cast<int>(t - static_cast<int64_t>(c.b) * p.segs);
+  return c;
+}
+
+__device__ __forceinline__ void task_step(const BwF32Params &p, TaskPos &c) {
+  if (++c.sg < p.segs) return;
+  c.sg = 0;
+  if (++c.b < p.n_blocks) return;
+  c.b = 0;
+  if (++c.h < p.H) return;
+  c.h = 0;
+  ++c.seq;
+}
+
+template <int kRows, int D>
+__device__ __forceinline__ Task task_at(const BwF32Params &p, const TaskPos &c) {
+  const int64_t b = c.b;
+  const int64_t first = b * p.block + static_cast<int64_t>(c.sg) * kRows;
   int64_t last = first + kRows;
   if (last > (b + 1) * p.block) last = (b + 1) * p.block;
   if (last > p.n) last = p.n;
   const int64_t l = (b - p.look_back) * p.block;
   const int64_t hh = (b + 1 + p.look_ahead) * p.block;
   Task k;
-  k.off = seq * p.n * p.row_stride + h * D;
-  k.seq = static_cast<int>(seq);
-  k.h = static_cast<int>(h);
+  k.off = static_cast<int64_t>(c.seq) * p.n * p.row_stride + static_cast<int64_t>(c.h) * D;
+  k.seq = c.seq;
+  k.h = c.h;
   k.row_lo = static_cast<int>(first);
   k.row_hi = static_cast<int>(last);
   k.lo = static_cast<int>(l > 0 ? l : 0);
@@ -170,7 +195,8 @@ __global__ void __launch_bounds__(kThreads)
   // ---- producer cursor: stage `is` of task `it` (0: q rows, 1..: K/V) ----
   int64_t it = t_begin;
   int is = 0;
-  Task ti = task_of<kRows, D>(p, it);
+  TaskPos pi = task_pos(p, it);
+  Task ti = task_at<kRows, D>(p, pi);
   int slot_in = 0;
   uint32_t issued = 0;   // stages issued by this warp
   auto issue_next = [&]() {
@@ -194,7 +220,10 @@ __global__ void __launch_bounds__(kThreads)
       ++issued;
       if (++is > kv_stages<kStage>(ti)) {
         is = 0;
-        if (++it < t_end) ti = task_of<kRows, D>(p, it);
+        if (++it < t_end) {
+          task_step(p, pi);
+          ti = task_at<kRows, D>(p, pi);
+        }
       }
     }
     slot_in = slot_in + 1 == kBuf ? 0 : slot_in + 1;
@@ -219,6 +248,7 @@ __global__ void __launch_bounds__(kThreads)
   float2 q2[kRL][2 * kF4], acc2[kRL][2 * kF4];
   float m[kRL], l[kRL];
   Task tc{0, 0, 0, 0, 0, 0, 0};
+  TaskPos pc = task_pos(p, t_begin);   // the consumer's current task
   int cs = 0, n_kv = 0, slot = 0;
   uint32_t consumed = 0;   // stages consumed by this warp
   bool ok = true;
@@ -234,7 +264,7 @@ __global__ void __launch_bounds__(kThreads)
     issue_next();          // refills the slot consumed last round
     float *cur = ring + slot * kSlot;
     if (cs == 0) {
-      tc = task_of<kRows, D>(p, ct);
+      tc = task_at<kRows, D>(p, pc);
       n_kv = kv_stages<kStage>(tc);
       const float2 s2 = make_float2(p.q_scale, p.q_scale);
 #pragma unroll
@@ -443,6 +473,7 @@ __global__ void __launch_bounds__(kThreads)
       }
       cs = 0;
       ++ct;
+      task_step(p, pc);
     } else {
       ++cs;
     }
@@ -504,8 +535,11 @@ cudaError_t launch_f32(BwF32Params p, const float *q, const float *k, const floa
     __atomic_store_n(&resident[dev & 63], per_sm, __ATOMIC_RELAXED);
   }
   const int64_t segs = (p.block + kRows - 1) / kRows;
+  const int64_t n_blocks = (static_cast<int64_t>(p.n) + p.block - 1) / p.block;
   p.H = H;
-  p.tasks_per_row = ((static_cast<int64_t>(p.n) + p.block - 1) / p.block) * segs;
+  p.n_blocks = static_cast<int>(n_blocks);   // <= n
+  p.segs = static_cast<int>(segs);           // <= block / kRows + 1
+  p.tasks_per_row = n_blocks * segs;
   p.n_tasks = p.tasks_per_row * H * batch;
   // every warp resident at once: each takes an equal run of tasks
   const int64_t warps = static_cast<int64_t>(sms) * per_sm * kWarps;
@@ -539,8 +573,16 @@ extern "C" pa_status pa_block_window_attn_fwd_f32(const float *q, const float *k
   int sms;
   cudaError_t e = device_context(&status, &sms);
   if (e != cudaSuccess) return from_cuda(e);
-  BwF32Params p{out, static_cast<int64_t>(H) * D, q_scale, n, block, look_back, look_ahead,
-                H, 0, 0, 0, status};
+  BwF32Params p{};
+  p.out = out;
+  p.row_stride = static_cast<int64_t>(H) * D;
+  p.q_scale = q_scale;
+  p.n = n;
+  p.block = block;
+  p.look_back = look_back;
+  p.look_ahead = look_ahead;
+  p.H = H;
+  p.status = status;
   auto st = reinterpret_cast<cudaStream_t>(stream);
   return from_cuda(D == 64 ? launch_f32<64>(p, q, k, v, batch, H, sms, st)
                            : launch_f32<128>(p, q, k, v, batch, H, sms, st));
