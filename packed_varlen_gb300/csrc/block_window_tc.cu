@@ -39,7 +39,8 @@
 //                 stores bf16.
 // TMEM per slot: S at [0, N), P over [0, N/2), O at [o_off, o_off + D) with
 // o_off >= N/2, so P and O live inside the columns S used and a slot costs
-// max(N, o_off + D) columns.  Keys outside [0, n) are zero-filled by TMA and
+// max(N, o_off + D) columns (long windows at D = 128: O after S, where it
+// accumulates over the chunks).  Keys outside [0, n) are zero-filled by TMA and
 // never inside any row's interval.  Every wait is bounded.
 //
 // The kernel is launched with programmatic stream serialization: it starts
@@ -187,6 +188,13 @@ __global__ void __launch_bounds__(kThreads, 1)
     block_window_tc_kernel(const __grid_constant__ CUtensorMap tm_q,
                            const __grid_constant__ CUtensorMap tm_k,
                            const __grid_constant__ CUtensorMap tm_v, const BwTcParams p) {
+  // long windows at D = 128: the running output of the chunks stays in TMEM
+  // (after S in the slot), accumulated by the PV MMAs; 128 fp32 registers
+  // per thread would spill
+  constexpr bool kOInTmem = kMulti && D == 128;
+  // D = 128 reads O for the epilogue 32 columns at a time (all 128 at once
+  // would spill); D = 64 reads its 64 columns in one go
+  constexpr bool kOPieces = D == 128;
   extern __shared__ uint8_t smem_raw[];
   if (threadIdx.x == 0) {   // descriptor fetches overlap the set-up below
     tma_prefetch_desc(&tm_q);
@@ -356,13 +364,15 @@ __global__ void __launch_bounds__(kThreads, 1)
       }
       issued = true;
     };
-    auto issue_pv = [&](int s, uint32_t d_s) {
+    // acc: the first MMA adds to O (a running output in TMEM) instead of
+    // overwriting it
+    auto issue_pv = [&](int s, uint32_t d_s, bool acc) {
       const uint32_t slot = base + s * p.slot_bytes;
       const uint64_t vdesc = sdesc_sw128(slot + p.v_off, D == 128 ? N * 128 : 1024, 1024);
       for (int kk = 0; kk < N / 16; ++kk) {
         if (lead)
           mma_ts(d_s + p.o_off, d_s + kk * 8, vdesc + ((kk * 16 * 128) >> 4), p.idesc_o,
-                 kk > 0 ? 1u : 0u);
+                 (kk > 0 || acc) ? 1u : 0u);
       }
     };
     if constexpr (!kMulti) {
@@ -390,7 +400,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           fence_after_sync();
-          issue_pv(s, tmem + s * p.slot_cols);
+          issue_pv(s, tmem + s * p.slot_cols, false);
           issued = true;
           if (lead) {
             mma_commit(bar(s, kOFull));
@@ -426,7 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             break;
           }
           fence_after_sync();
-          issue_pv(s, d_s);
+          issue_pv(s, d_s, kOInTmem && c > 0);
           if (lead) {
             mma_commit(bar(s, kOFull));
             mma_commit(bar(s, kKvEmpty));
@@ -475,7 +485,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       __nv_bfloat16 *dst =
           p.out + ((static_cast<int64_t>(it.bi) * p.n + (valid ? i : 0)) * p.H + it.h) * D;
       float m_run = -INFINITY, l_run = 0.f;
-      float acc[kMulti ? D : 1];
+      float acc[kMulti && !kOInTmem ? D : 1];
       for (int c = 0; c < it.nc; ++c) {
         const uint32_t u = kMulti ? cnt_get(kvc, s) : static_cast<uint32_t>(li / ns);
         // this row's columns [a, e) of the chunk, the warp's union in 32-column
@@ -549,6 +559,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         const float m_use = m_new == -INFINITY ? 0.f : m_new;
         const float alpha = ex2((m_run - m_use) * mul);   // 0 while nothing was seen
         const float negm = -m_use * mul;
+        if constexpr (kOInTmem) {
+          // the running O (chunks before c; their PVs are done, waited for
+          // below) brought to the new maximum before this chunk's PV adds to it
+          if (c > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+#pragma unroll 1
+            for (int cc = 0; cc < D / 32; ++cc) {
+              uint32_t r[32];
+              tmem_ld32(lane_base + col_o + cc * 32, r);
+              tmem_wait_ld();
+#pragma unroll
+              for (int j = 0; j < 32; ++j) r[j] = __float_as_uint(__uint_as_float(r[j]) * alpha);
+              tmem_st32(lane_base + col_o + cc * 32, r);
+            }
+          }
+        }
         // P of keys [32 i, 32 i + 32) goes to P columns [16 i, 16 i + 16),
         // which hold S columns of pieces <= i, read before the store; outside
         // the union P is 0 (stored after every read of the union, since those
@@ -624,6 +649,43 @@ __global__ void __launch_bounds__(kThreads, 1)
           break;
         }
         fence_after_sync();
+        if constexpr (kOPieces) {
+          // O / l of the last chunk, 32 columns at a time
+          if (c == it.nc - 1) {
+            if (!waited) {
+              griddep_wait();
+              waited = true;
+            }
+            const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
+#pragma unroll 1
+            for (int cc = 0; cc < D / 32; ++cc) {
+              uint32_t r[32];
+              tmem_ld32(lane_base + col_o + cc * 32, r);
+              tmem_wait_ld();
+              if (valid) {
+                uint4 *d4 = reinterpret_cast<uint4 *>(dst + cc * 32);
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                  uint4 w;
+                  w.x = pack_bf16x2(__uint_as_float(r[8 * v + 0]) * inv,
+                                    __uint_as_float(r[8 * v + 1]) * inv);
+                  w.y = pack_bf16x2(__uint_as_float(r[8 * v + 2]) * inv,
+                                    __uint_as_float(r[8 * v + 3]) * inv);
+                  w.z = pack_bf16x2(__uint_as_float(r[8 * v + 4]) * inv,
+                                    __uint_as_float(r[8 * v + 5]) * inv);
+                  w.w = pack_bf16x2(__uint_as_float(r[8 * v + 6]) * inv,
+                                    __uint_as_float(r[8 * v + 7]) * inv);
+                  d4[v] = w;
+                }
+              }
+            }
+          }
+          fence_before_sync();
+          mbar_arrive(bar(s, kTFree));   // S and P may take the next chunk or item
+          m_run = m_new;
+          cnt_add(kvc, s, 1u);
+          continue;
+        }
         uint32_t o[D / 32][32];
 #pragma unroll
         for (int cc = 0; cc < D / 32; ++cc) tmem_ld32(lane_base + col_o + cc * 32, o[cc]);
@@ -655,7 +717,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               }
             }
           }
-        } else if constexpr (kMulti) {
+        } else if constexpr (kMulti && !kOInTmem) {
 #pragma unroll
           for (int cc = 0; cc < D / 32; ++cc)
 #pragma unroll
@@ -667,7 +729,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if constexpr (kMulti) cnt_add(kvc, s, 1u);
       }
       if (!ok) break;
-      if constexpr (kMulti) {
+      if constexpr (kMulti && !kOInTmem) {
         if (it.nc > 1 && valid) {
           const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
           uint4 *d4 = reinterpret_cast<uint4 *>(dst);
@@ -726,8 +788,15 @@ bool plan(const BlockWindowArgs &a, BwTcParams &p) {
   long long W = (span + a.look_back + a.look_ahead) * static_cast<long long>(a.block);
   if (W > a.n) W = a.n;
   p.N = W >= kMaxN ? kMaxN : round_up(static_cast<int>(W), 16);
-  p.o_off = round_up(p.N / 2, 32);
-  p.slot_cols = round_up(p.N > p.o_off + D ? p.N : p.o_off + D, 32);
+  const bool multi = W > p.N;
+  if (multi && D == 128) {
+    // the running output stays in TMEM across chunks: after S, not inside it
+    p.o_off = round_up(p.N, 32);
+    p.slot_cols = p.o_off + D;
+  } else {
+    p.o_off = round_up(p.N / 2, 32);
+    p.slot_cols = round_up(p.N > p.o_off + D ? p.N : p.o_off + D, 32);
+  }
   const int q_bytes = kM * D * 2, kv = p.N * D * 2;
   p.slot_bytes = q_bytes + 2 * kv;
   p.k_off = q_bytes;
@@ -743,7 +812,7 @@ bool plan(const BlockWindowArgs &a, BwTcParams &p) {
   p.bar_off = p.nslots * p.slot_bytes;
   p.idesc_s = idesc_bf16_f32(kM, p.N, false);
   p.idesc_o = idesc_bf16_f32(kM, D, true);
-  return W > p.N;
+  return multi;
 }
 
 template <int D, bool kMulti>

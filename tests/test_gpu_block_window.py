@@ -180,3 +180,21 @@ def test_chained_layers_respect_stream_order(pv):
     assert torch.equal(chain_in_place(False).view(torch.int16),
                        chain_in_place(True).view(torch.int16))
     assert pv.get_device_status() == 0
+
+
+@pytest.mark.parametrize("D", [64, 128])
+def test_multi_chunk_rescale_on_growing_scores(pv, D):
+    # windows of up to 700 keys are taken in 256-key chunks; keys of later
+    # chunks are scaled up so that rows' maxima grow from chunk to chunk and
+    # the running output (in TMEM at D = 128, in registers at D = 64) is
+    # rescaled before each later chunk's PV
+    w = workloads.random_block_window(1, 700, 2, D, 100, seed=77 + D)
+    k = w.k.clone()
+    grow = (1.0 + 1.5 * (torch.arange(700) // 256).float()).to(torch.bfloat16)
+    k = (k.float() * grow.float()[None, :, None, None]).to(torch.bfloat16)
+    w2 = workloads.BlockWindowWorkload("growing", 1, 700, 2, D, 100, [(3, 3)], w.q, k, w.v, w.seed)
+    for lb, la in [(3, 3), (6, 0), (0, 6)]:
+        got = oracle.to_f64(_run(pv, w2, lb, la))
+        want = oracle.block_window_attention(w.q, k, w.v, 100, lb, la, w.scale)
+        assert_close_to_oracle(got, want, f"D={D} look=({lb},{la})")
+    assert pv.get_device_status() == 0
