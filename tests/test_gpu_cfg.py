@@ -55,9 +55,12 @@ def _small(C, normalize):
     return seg
 
 
-@pytest.mark.parametrize("C", [8, 64, 3072])
+@pytest.mark.parametrize("C", [8, 64, 136, 256, 1000, 3072])
 @pytest.mark.parametrize("normalize", [0, 1])
 def test_small_layouts(pv, C, normalize):
+    # rows of 1, 8, 17, 32, 125 and 384 sixteen-byte vectors: several rows per
+    # warp, one row per warp with fewer vectors than lanes, exactly one vector
+    # per lane, and ragged last batches of the four vectors a lane loads at once
     seg = _small(C, normalize)
     got = _gpu(pv, seg, out_fill=5.0)
     want = oracle.cfg_combine(seg.flat, seg.lengths, seg.text, seg.pos_seq, seg.neg_seq,
