@@ -194,3 +194,14 @@ def test_graph_replay_matches_eager(pv):
     torch.cuda.synchronize()
     for a, b in zip(eager, outs):
         assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+@pytest.mark.parametrize("block", [14, 15, 16, 17, 18, 19, 21, 22, 23])
+def test_every_partial_stage_length(pv, block):
+    # keys come in stages of 12; an own-block window of 14-23 keys leaves
+    # 2-11 valid keys in its last stage (and the sequence's last block fewer)
+    n = 4 * block + 5
+    w = workloads.random_block_window_f32(1, n, 2, 64, block, seed=block)
+    for lb, la in [(0, 0), (1, 0)]:
+        want = oracle.block_window_attention(w.q, w.k, w.v, block, lb, la, w.scale)
+        _close(_run(pv, w, lb, la), want, f"block={block} look=({lb},{la})")
