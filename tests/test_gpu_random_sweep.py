@@ -1,0 +1,92 @@
+"""Seeded random sweeps: many small shapes drawn from fixed seeds, each
+compared element by element with the fp64 oracle through the C ABI.
+
+The hand-picked cases in the other files aim at known edges; these draw
+lengths, head counts, head dims, blocks and looks at random (within sizes the
+oracle computes in a moment), so that combinations nobody listed are also
+checked: varlen batches with cross lengths and empty sequences, and block
+windows in bf16 and fp32 with any block, look and partial last block."""
+import numpy as np
+import pytest
+
+import oracle
+import workloads
+from helpers import assert_close_to_oracle, gpu_varlen
+
+pytestmark = pytest.mark.gpu
+
+F32_MAX_ABS = 6e-6
+F32_MEAN_ABS = 5e-7
+
+
+@pytest.fixture(scope="module")
+def pv():
+    import packed_varlen_gb300 as pv
+    pv.load_library()
+    pv.get_device_status()
+    return pv
+
+
+def _varlen_case(seed):
+    rng = np.random.default_rng(1000 + seed)
+    B = int(rng.integers(1, 7))
+    D = int(rng.choice([64, 128]))
+    H = int(rng.integers(1, 4))
+    lq = [int(x) for x in rng.integers(0, 400, size=B)]
+    cross = bool(rng.integers(0, 2))
+    lk = [int(x) for x in rng.integers(0, 400, size=B)] if cross else None
+    if sum(lq) == 0:
+        lq[0] = 1
+    return lq, lk, H, D
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_varlen_random_shapes(pv, seed):
+    lq, lk, H, D = _varlen_case(seed)
+    w = workloads.random_varlen(lq, lk, H, D, seed=seed)
+    out, cu_q, cu_k = gpu_varlen(pv, w)
+    ocq = oracle.cu_seqlens_from_lengths(w.lengths_q)
+    ock = oracle.cu_seqlens_from_lengths(w.lengths_k)
+    want = oracle.varlen_attention(w.q, w.k, w.v, ocq, ock, w.scale)
+    T = int(ocq[-1])
+    assert_close_to_oracle(oracle.to_f64(out)[:T], want[:T], f"seed={seed} Lq={lq} Lk={lk}")
+    assert pv.get_device_status() == 0
+
+
+def _window_case(seed):
+    rng = np.random.default_rng(2000 + seed)
+    block = int(rng.choice([1, 3, 8, 13, 20, 24, 31, 32, 40, 64, 100]))
+    n = int(rng.integers(1, 6 * block + 200))
+    look = (int(rng.integers(0, 4)), int(rng.integers(0, 4)))
+    batch = int(rng.integers(1, 3))
+    H = int(rng.integers(1, 4))
+    D = int(rng.choice([64, 128]))
+    return block, n, look, batch, H, D
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_block_window_random_shapes(pv, seed):
+    block, n, look, batch, H, D = _window_case(seed)
+    w = workloads.random_block_window(batch, n, H, D, block, seed=seed)
+    q, k, v = w.q.cuda(), w.k.cuda(), w.v.cuda()
+    got = pv.block_window_attn_fwd(q, k, v, block, look[0], look[1], scale=w.scale)
+    want = oracle.block_window_attention(w.q, w.k, w.v, block, look[0], look[1], w.scale)
+    assert_close_to_oracle(oracle.to_f64(got.cpu()), want,
+                           f"seed={seed} block={block} n={n} look={look} D={D}")
+    assert pv.get_device_status() == 0
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_block_window_f32_random_shapes(pv, seed):
+    block, n, look, batch, H, D = _window_case(seed + 100)
+    w = workloads.random_block_window_f32(batch, n, H, D, block, seed=seed)
+    q, k, v = w.q.cuda(), w.k.cuda(), w.v.cuda()
+    got = oracle.to_f64(pv.block_window_attn_fwd_f32(q, k, v, block, look[0], look[1],
+                                                     scale=w.scale).cpu())
+    want = oracle.block_window_attention(w.q, w.k, w.v, block, look[0], look[1], w.scale)
+    err = np.abs(got - want)
+    what = f"seed={seed} block={block} n={n} look={look} D={D}"
+    assert np.isfinite(got).all(), what
+    assert err.max() <= F32_MAX_ABS, f"{what}: max abs {err.max():.3e}"
+    assert err.mean() <= F32_MEAN_ABS, f"{what}: mean abs {err.mean():.3e}"
+    assert pv.get_device_status() == 0
