@@ -4,8 +4,9 @@ compared element by element with the fp64 oracle through the C ABI.
 The hand-picked cases in the other files aim at known edges; these draw
 lengths, head counts, head dims, blocks and looks at random (within sizes the
 oracle computes in a moment), so that combinations nobody listed are also
-checked: varlen batches with cross lengths and empty sequences, and block
-windows in bf16 and fp32 with any block, look and partial last block."""
+checked: varlen batches with cross lengths and empty sequences, block
+windows in bf16 and fp32 with any block, look and partial last block, and
+the packed-M linear layer with ragged M, N and K."""
 import numpy as np
 import pytest
 
@@ -89,4 +90,28 @@ def test_block_window_f32_random_shapes(pv, seed):
     assert np.isfinite(got).all(), what
     assert err.max() <= F32_MAX_ABS, f"{what}: max abs {err.max():.3e}"
     assert err.mean() <= F32_MEAN_ABS, f"{what}: mean abs {err.mean():.3e}"
+    assert pv.get_device_status() == 0
+
+
+def _linear_case(seed):
+    rng = np.random.default_rng(3000 + seed)
+    M = int(rng.integers(1, 700))
+    N = 8 * int(rng.integers(1, 150))
+    K = 8 * int(rng.integers(1, 80))
+    return M, N, K, bool(rng.integers(0, 2))
+
+
+@pytest.mark.parametrize("seed", range(40))
+def test_linear_random_shapes(pv, seed):
+    # bound: one bf16 rounding of the result plus an fp32 accumulation
+    # allowance of 2^-14 * sum_k |x_k w_k| (as the linear layer's own tests)
+    M, N, K, with_bias = _linear_case(seed)
+    c = workloads.linear_case([M], N, K, seed=seed, bias=with_bias)
+    y = pv.linear_bf16(c.x.cuda(), c.w.cuda(), None if c.bias is None else c.bias.cuda()).cpu()
+    want = oracle.linear(c.x, c.w, c.bias)
+    absdot = np.abs(oracle.to_f64(c.x)) @ np.abs(oracle.to_f64(c.w)).T
+    if c.bias is not None:
+        absdot = absdot + np.abs(oracle.to_f64(c.bias))[None, :]
+    excess = np.abs(oracle.to_f64(y) - want) - (2.0 ** -8 * np.abs(want) + 2.0 ** -14 * absdot)
+    assert excess.max() <= 0, f"seed={seed} M={M} N={N} K={K}: max excess {excess.max():.3e}"
     assert pv.get_device_status() == 0
