@@ -5,8 +5,9 @@ The hand-picked cases in the other files aim at known edges; these draw
 lengths, head counts, head dims, blocks and looks at random (within sizes the
 oracle computes in a moment), so that combinations nobody listed are also
 checked: varlen batches with cross lengths and empty sequences, block
-windows in bf16 and fp32 with any block, look and partial last block, and
-the packed-M linear layer with ragged M, N and K."""
+windows in bf16 and fp32 with any block, look and partial last block, the
+packed-M linear layer with ragged M, N and K, pack/unpack (bit-exact) and
+request-local RoPE with random offsets and bases."""
 import numpy as np
 import pytest
 
@@ -114,4 +115,57 @@ def test_linear_random_shapes(pv, seed):
         absdot = absdot + np.abs(oracle.to_f64(c.bias))[None, :]
     excess = np.abs(oracle.to_f64(y) - want) - (2.0 ** -8 * np.abs(want) + 2.0 ** -14 * absdot)
     assert excess.max() <= 0, f"seed={seed} M={M} N={N} K={K}: max excess {excess.max():.3e}"
+    assert pv.get_device_status() == 0
+
+
+def _rows_case(seed, base_seed):
+    rng = np.random.default_rng(base_seed + seed)
+    B = int(rng.integers(1, 7))
+    lengths = [int(x) for x in rng.integers(0, 300, size=B)]
+    H = int(rng.integers(1, 5))
+    D = int(rng.choice([8, 16, 64, 128]))
+    return lengths, H, D, rng
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_pack_unpack_random_shapes(pv, seed):
+    # bit-exact: padded -> flat -> padded, padding rows of the target kept
+    import torch
+    lengths, H, D, _ = _rows_case(seed, 4000)
+    if sum(lengths) == 0:   # (empty buffers have null pointers; not this test's case)
+        lengths[0] = 1
+    pw = workloads.padded(lengths, H, D, seed=seed)
+    cu = pv.cu_seqlens_from_lengths(torch.tensor(lengths, dtype=torch.int32, device="cuda"))
+    i16 = lambda t: t.view(torch.int16).cpu().numpy()
+    flat = pv.pack(pw.q.cuda(), cu, sum(lengths))
+    want = oracle.pack(i16(pw.q), lengths)
+    assert np.array_equal(i16(flat), want), f"seed={seed} L={lengths}"
+    target = torch.full_like(pw.q, -2.0).cuda()
+    pv.unpack(flat, cu, target)
+    want_pad = oracle.unpack(want, lengths, i16(torch.full_like(pw.q, -2.0)))
+    assert np.array_equal(i16(target), want_pad), f"seed={seed} L={lengths}"
+    assert pv.get_device_status() == 0
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_rope_random_shapes(pv, seed):
+    # within one bf16 rounding of a result computed to ~1e-5 of its pair's norm
+    import torch
+    lengths, H, D, rng = _rows_case(seed, 5000)
+    if sum(lengths) == 0:
+        lengths[0] = 1
+    offsets = [int(x) for x in rng.integers(0, 5000, size=len(lengths))]
+    base = float(rng.choice([500.0, 1e4, 1e6]))
+    w = workloads.random_varlen(lengths, None, H, D, seed=seed)
+    dev = "cuda"
+    cu = pv.cu_seqlens_from_lengths(torch.tensor(lengths, dtype=torch.int32, device=dev))
+    q, k = w.q.to(dev), w.k.to(dev)
+    pv.rope_packed(q, k, cu, cu, torch.tensor(offsets, dtype=torch.int32, device=dev), base)
+    pos = oracle.rope_positions(lengths, offsets)
+    for got, x in ((q.cpu(), w.q), (k.cpu(), w.k)):
+        want = oracle.rope(x, pos, base)
+        xx = oracle.to_f64(x)
+        pair = np.repeat(np.hypot(xx[..., 0::2], xx[..., 1::2]), 2, axis=-1)
+        excess = np.abs(oracle.to_f64(got) - want) - (2.0 ** -8 * np.abs(want) + 1e-5 * pair)
+        assert excess.max() <= 0, f"seed={seed} L={lengths} D={D}: {excess.max():.3e}"
     assert pv.get_device_status() == 0
